@@ -23,6 +23,7 @@ import json
 import os
 import platform
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -119,7 +120,7 @@ class Clocks:
         self.index = index
         self.uuid = uuid
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"dflash_clocks_{os.getpid()}_rank{index}.csv")
 
     def start(self):
         try:

@@ -802,6 +802,17 @@ int copy_out(void* dst, const void* src, size_t bytes, cudaStream_t s) {
 // Split-KV workspace of n rows of 128 outputs + 1 log-sum-exp, with room for
 // twice the splits: the split count follows the host's upper bound of the
 // context, which grows between an eager call and a capture.
+// With a caller-provided split-KV scratch (the no-allocation draft), the most
+// KV splits whose partials fit it: `per_split` rows of 128 outputs + 1
+// log-sum-exp each.  One split needs no scratch at all (the attention writes
+// its output directly), so a draft never fails for want of scratch; it only
+// runs with fewer, longer splits.
+int clamp_splits_to_scratch(const dflash_ctx* c, int n_splits, size_t per_split) {
+  if (c->attn_scratch_ext == nullptr || n_splits <= 1) return n_splits;
+  const size_t fit = c->attn_scratch_ext_floats / (per_split * 129);
+  return (int)std::max<size_t>(1, std::min<size_t>((size_t)n_splits, fit));
+}
+
 int attn_workspace(dflash_ctx* c, size_t n, float** part_o, float** part_lse, cudaStream_t s) {
   if (c->attn_scratch_ext != nullptr) {
     if (n * 129 > c->attn_scratch_ext_floats)
@@ -858,6 +869,7 @@ int run_attention_umma(dflash_ctx* c, const void* qb, void* ob, int l, int R, cu
   tiles_total *= (int64_t)p.n_kv * p.n_qtiles;
   const int64_t per_cta = std::max<int64_t>(2, (tiles_total + c->num_sms - 1) / c->num_sms);
   p.n_splits = (int)std::max<int64_t>(1, std::min<int64_t>(64, (max_tiles + per_cta - 1) / per_cta));
+  p.n_splits = clamp_splits_to_scratch(c, p.n_splits, (size_t)c->B * p.n_kv * p.rows_pad);
   if (c->B > 1) p.seq_order = c->d_seq_order;   // longest contexts first (ordered once per draft)
   if (p.n_splits > 1)
     RET(attn_workspace(c, (size_t)c->B * p.n_kv * p.n_splits * p.rows_pad, &p.part_o, &p.part_lse, s));
@@ -916,6 +928,7 @@ int run_attention(dflash_ctx* c, const T* qb, T* ob, int l, int R, cudaStream_t 
   tiles_total *= (int64_t)p.n_kv * p.n_qtiles;
   const int64_t per_cta = std::max<int64_t>(2, (tiles_total + 2 * c->num_sms - 1) / (2 * c->num_sms));
   p.n_splits = (int)std::max<int64_t>(1, std::min<int64_t>(64, (max_tiles + per_cta - 1) / per_cta));
+  p.n_splits = clamp_splits_to_scratch(c, p.n_splits, (size_t)c->B * p.n_kv * p.rows_pad);
   if (p.n_splits > 1) {
     const size_t n = (size_t)c->B * p.n_kv * p.n_splits * p.rows_pad;
     if (c->attn_scratch_ext != nullptr) {

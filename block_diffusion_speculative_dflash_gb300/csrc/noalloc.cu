@@ -12,18 +12,24 @@
 // log-sum-exps -- takes that scratch from the file-scope static device array
 // below instead of a context workspace, and every context workspace stays at
 // its current size (a draft that would need a larger one fails with
-// DFLASH_ERR_CAPACITY instead of allocating).  Results are identical to
-// dflash_draft_block's.
+// DFLASH_ERR_CAPACITY instead of allocating).  When the split count the draft
+// would pick does not fit the array, the attention runs with as many splits as
+// fit (down to one split, which needs no scratch), so the ids and logits agree
+// with dflash_draft_block's up to the summation order of the split-KV merge
+// (fp32 rounding), not bit for bit.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "dflash.h"
 
-// Capacity of the static split-KV scratch: 2M floats = 8 MiB, enough for
-// batch x kv_heads x splits x query rows x 129 floats up to e.g. 8 KV heads x
-// 17 splits x 80 rows x 16 sequences.  Every GPU that loads the library holds
-// this array until the process exits.
+// Capacity of the static split-KV scratch: 2M floats = 8 MiB.  A draft needs
+// batch x kv_heads x splits x rows_pad x 129 floats, rows_pad being the query
+// rows of a KV head rounded up to 128 (G query heads x (K + 1) block rows); for
+// one sequence of 8 KV heads with K + 1 <= 32 block rows of 4 query heads that
+// is 8 x 128 x 129 floats per split, so up to 15 splits fit.  Every GPU that
+// loads the library holds this array until the process exits.
 constexpr size_t kScratchFloats = (size_t)2 << 20;
 static __device__ __align__(256) float g_split_kv_scratch[kScratchFloats];
 
@@ -35,11 +41,33 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+// the array's device address per device, valid for the CUDA context current
+// when it was looked up (a reset device gets a new context and a new module
+// load, so the address is looked up again)
 float* g_addr[kMaxDevices] = {};
+CUcontext g_addr_ctx[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static bool looked = false;
+  if (!looked) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    cudaGetLastError();
+    looked = true;
+  }
+  return fn;
+}
 
 // Device address of the static scratch on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device (with that device current) and cached.
+// with cudaGetSymbolAddress (with the device current) the first time a device
+// -- or a new context on it -- calls, and reused while that context lives.
 int scratch_address(float** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -47,7 +75,10 @@ int scratch_address(float** out) {
     return dfl_fail(DFLASH_ERR_CUDA, "cannot determine the current device");
   }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_addr[dev] == nullptr) {
+  CUcontext cur = nullptr;
+  const CtxGetCurrentFn get = ctx_get_current();
+  if (get == nullptr || get(&cur) != CUDA_SUCCESS) cur = nullptr;
+  if (g_addr[dev] == nullptr || cur == nullptr || cur != g_addr_ctx[dev]) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_split_kv_scratch);
     if (e != cudaSuccess || p == nullptr) {
@@ -55,6 +86,8 @@ int scratch_address(float** out) {
       return dfl_fail(DFLASH_ERR_CUDA, "cudaGetSymbolAddress of the static split-KV scratch failed");
     }
     g_addr[dev] = static_cast<float*>(p);
+    if (cur == nullptr && get != nullptr && get(&cur) != CUDA_SUCCESS) cur = nullptr;
+    g_addr_ctx[dev] = cur;   // null: unknown context, looked up again next call
   }
   *out = g_addr[dev];
   return DFLASH_OK;

@@ -215,14 +215,20 @@ int dflash_draft_block_k(dflash_ctx* ctx, const int32_t* anchor_ids, int32_t K, 
  * cudaMalloc is an error; a process whose device memory is carved up once at
  * start-up).  The pages have no counterpart: this is a deployment variant.
  * The attention's split-KV scratch comes from a static device array of 8 MiB
- * held by every GPU that loads the library; a draft whose split-KV scratch
- * would exceed it, or that would need any context workspace to grow (run one
- * dflash_draft_block with the same K and batch first), fails with
- * DFLASH_ERR_CAPACITY and allocates nothing.  The first call on a device looks
- * up the array's device address (with lazy module loading this is also when the
- * array's 8 MiB appear on that device), so make it before any stream capture.  All
- * calls share the array: calls that overlap on the GPU (other streams, other
- * contexts) race on it.  Arguments and results as for dflash_draft_block. */
+ * (2M floats) held by every GPU that loads the library.  A draft needs
+ * batch x kv_heads x splits x rows_pad x 129 floats of it (rows_pad: the query
+ * rows of a KV head, G x (K + 1), rounded up to 128 on the tensor-core path);
+ * when the split count the draft would choose does not fit, it runs with as
+ * many splits as fit (one split needs none), so its ids and logits agree with
+ * dflash_draft_block's up to the fp32 summation order of the split merge.  A
+ * draft that would need any context workspace to grow (run one
+ * dflash_draft_block with the same K and batch first) fails with
+ * DFLASH_ERR_CAPACITY and allocates nothing.  The first call on a device (or
+ * on a new context of it) looks up the array's device address (with lazy
+ * module loading this is also when the array's 8 MiB appear on that device),
+ * so make it before any stream capture.  All calls share the array: calls that
+ * overlap on the GPU (other streams, other contexts) race on it.  Arguments and
+ * results as for dflash_draft_block. */
 int dflash_draft_block_noalloc(dflash_ctx* ctx, const int32_t* anchor_ids, int32_t K,
                                int32_t* draft_ids, float* logits, void* stream);
 

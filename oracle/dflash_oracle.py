@@ -43,24 +43,6 @@ reading taken (all readings are listed in the design notes):
     [UPJ メタデータの同期]: the context buffer, KV positions and RoPE offset
     advance by the truly accepted count, never by the verified block length.
 
-Storage precision.  `act_dtype="f64"` (default) is the exact definition.
-`act_dtype="bf16"` computes the same definition but rounds, to bf16 with
-round-to-nearest-even, exactly the intermediate values that the CUDA path
-stores in bf16 between its kernels: the context feature u, the K/V cache rows,
-the normalised inputs of every projection (attention and MLP), the rotated
-queries, the attention output, the SwiGLU product and the final normalised
-rows.  It exists because an argmax decided in floating point is compared with
-both sides taking the decision in the same precision (the kernel's, the pages
-fixing none); logits are checked against the exact mode.  Where the CUDA path
-folds an RMSNorm into the projection that follows it -- RMSNorm(h) W^T equals
-diag(1/rms(h)) (h * g) W^T -- the stored value is h * g and the row scale is
-applied to the projection's output; the storage mode rounds at that point too
-(the context feature, the MLP input, the input of attention in every layer
-after the first, and the final norm).  The inputs of the projections (those
-operands, the attention output and the SwiGLU product) are stored split, as
-the sum of two bf16 values hi = bf16(x), lo = bf16(x - hi); the rotated queries
-and the K/V cache are stored in one bf16 value.
-
 Parity status: each function is pinned by the CPU tests (closed forms,
 invariants, library routines on special cases, brute force on tiny inputs).
 The full drafter's logits have no worked example on the pages, so the complete
@@ -218,17 +200,13 @@ class OracleDrafter:
     CONDITIONING = ("kv", "input", "none")
 
     def __init__(self, shape, weights: Dict[str, np.ndarray], batch: int,
-                 dtype=np.float64, pos_offset: int = 0, use_rope: bool = True, act_dtype: str = "f64",
-                 conditioning: str = "kv"):
+                 dtype=np.float64, pos_offset: int = 0, use_rope: bool = True, conditioning: str = "kv"):
         if conditioning not in self.CONDITIONING:
             raise ValueError(conditioning)
         self.cond = conditioning
         self.s = shape
         self.raw = weights
         self.dtype = dtype
-        if act_dtype not in ("f64", "bf16"):
-            raise ValueError(act_dtype)
-        self.act_bf16 = act_dtype == "bf16"   # round stored intermediates to bf16
         self.pos_offset = int(pos_offset)   # test hook: shifts every RoPE position
         self.use_rope = use_rope            # test hook: RoPE off for equivariance checks
         self.seqs = [SeqState(k=[np.zeros((0, shape.n_kv_heads, shape.head_dim), dtype)
@@ -247,28 +225,10 @@ class OracleDrafter:
                 self._cache[name] = a
         return a
 
-    def _st(self, x: np.ndarray) -> np.ndarray:
-        """A value the CUDA path stores between kernels (bf16 storage mode only)."""
-        return round_bf16(x).astype(self.dtype) if self.act_bf16 else x
-
-    def _st2(self, x: np.ndarray) -> np.ndarray:
-        """A projection input the CUDA path stores split: bf16(x) + bf16(x - bf16(x))."""
-        if not self.act_bf16:
-            return x
-        hi = round_bf16(x).astype(np.float64)
-        return (hi + round_bf16(np.asarray(x, np.float64) - hi)).astype(self.dtype)
-
-    def _norm_proj(self, h: np.ndarray, gain: np.ndarray, mats, folded: bool = True):
-        """[RMSNorm(h) W^T for W in mats].  In storage mode with `folded`, the
-        stored operand is h * gain and each output row is scaled by 1/rms(h)
-        afterwards (the same product, rounded where the CUDA path rounds)."""
-        eps = self.s.rms_eps
-        if not (self.act_bf16 and folded):
-            x = self._st2(rms_norm(h, gain, eps))
-            return [x @ W.T for W in mats]
-        inv = 1.0 / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + eps)
-        xs = self._st2(h * gain)
-        return [inv * (xs @ W.T) for W in mats]
+    def _norm_proj(self, h: np.ndarray, gain: np.ndarray, mats):
+        """[RMSNorm(h) W^T for W in mats]."""
+        x = rms_norm(h, gain, self.s.rms_eps)
+        return [x @ W.T for W in mats]
 
     def _rope(self, x: np.ndarray, pos: np.ndarray) -> np.ndarray:
         if not self.use_rope:
@@ -302,8 +262,8 @@ class OracleDrafter:
             k, v = self._norm_proj(y, self.w("fc_norm"), [self.w(p + "wk"), self.w(p + "wv")])
             k = k.reshape(rows, s.n_kv_heads, s.head_dim)
             v = v.reshape(rows, s.n_kv_heads, s.head_dim)
-            st.k[l] = np.concatenate([st.k[l], self._st(self._rope(k, pos))], axis=0)
-            st.v[l] = np.concatenate([st.v[l], self._st(v)], axis=0)
+            st.k[l] = np.concatenate([st.k[l], self._rope(k, pos)], axis=0)
+            st.v[l] = np.concatenate([st.v[l], v], axis=0)
         st.kv_len += rows
         st.ctx_len = max(st.ctx_len, st.kv_len)
 
@@ -345,7 +305,7 @@ class OracleDrafter:
         for l in range(s.n_layers):
             p = f"layers.{l}."
             q, k, v = self._norm_proj(h, self.w(p + "attn_norm"),
-                                      [self.w(p + "wq"), self.w(p + "wk"), self.w(p + "wv")], folded=l > 0)
+                                      [self.w(p + "wq"), self.w(p + "wk"), self.w(p + "wv")])
             q = q.reshape(Bs, R, s.n_q_heads, s.head_dim)
             k = k.reshape(Bs, R, s.n_kv_heads, s.head_dim)
             v = v.reshape(Bs, R, s.n_kv_heads, s.head_dim)
@@ -353,32 +313,21 @@ class OracleDrafter:
             for i, b in enumerate(seqs):
                 st = self.seqs[b]
                 pos = st.ctx_len + np.arange(R)
-                qb = self._st(self._rope(q[i], pos))
-                kb = self._st(self._rope(k[i], pos))
+                qb = self._rope(q[i], pos)
+                kb = self._rope(k[i], pos)
                 if self.cond == "kv":
                     keys = np.concatenate([st.k[l], kb], axis=0)
-                    vals = np.concatenate([st.v[l], self._st(v[i])], axis=0)
+                    vals = np.concatenate([st.v[l], v[i]], axis=0)
                 else:   # no context keys: the block attends to itself only
-                    keys, vals = kb, self._st(v[i])
+                    keys, vals = kb, v[i]
                 o[i] = attention(qb, keys, vals).reshape(R, s.q_dim)
-            h = h + self._st2(o) @ self.w(p + "wo").T
-            if self.act_bf16:
-                g, u = self._norm_proj(h, self.w(p + "mlp_norm"), [self.w(p + "w_gate"), self.w(p + "w_up")])
-                a = self._st2(silu(g) * u)
-                h = h + a @ self.w(p + "w_down").T
-            else:
-                x = rms_norm(h, self.w(p + "mlp_norm"), s.rms_eps)
-                h = h + swiglu(x, self.w(p + "w_gate"), self.w(p + "w_up"), self.w(p + "w_down"))
+            h = h + o @ self.w(p + "wo").T
+            x = rms_norm(h, self.w(p + "mlp_norm"), s.rms_eps)
+            h = h + swiglu(x, self.w(p + "w_gate"), self.w(p + "w_up"), self.w(p + "w_down"))
 
         hm = h[:, 1:, :].reshape(Bs * K, H)   # the K mask rows
-        if self.act_bf16:
-            inv = 1.0 / np.sqrt(np.mean(hm * hm, axis=-1, keepdims=True) + s.rms_eps)
-            xf = self._st2(hm * self.w("final_norm"))
-            logits = (inv * self.lm_head(xf)).reshape(Bs, K, s.vocab)
-            xf = inv * xf
-        else:
-            xf = rms_norm(hm, self.w("final_norm"), s.rms_eps)
-            logits = self.lm_head(xf).reshape(Bs, K, s.vocab)
+        xf = rms_norm(hm, self.w("final_norm"), s.rms_eps)
+        logits = self.lm_head(xf).reshape(Bs, K, s.vocab)
         xf = xf.reshape(Bs, K, H)
         drafts = greedy_argmax(logits)
         out = (drafts, logits if want_logits else None)

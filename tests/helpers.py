@@ -124,7 +124,11 @@ class SideBySide:
         if ks is not None:
             for b in range(B):
                 assert np.all(dg[b, kb[b]:] == -1), f"seq {b}: ids past K_b = {kb[b]} are not -1"
-        rep = {"it": it, "max_rel": 0.0, "max_abs": 0.0, "ids_compared": 0, "ids_equal": 0}
+        # ids_band: rows whose oracle top-2 gap exceeds 1e-2 but not twice the row's
+        # measured logit error -- compared under the plain 1e-2 rule, excluded by the
+        # error-aware one; ids_band_equal: how many of those agree all the same
+        rep = {"it": it, "max_rel": 0.0, "max_abs": 0.0, "ids_compared": 0, "ids_equal": 0,
+               "ids_band": 0, "ids_band_equal": 0}
         for k, i in enumerate(live):
             b = self.oseqs[i]
             n_b = int(kb[b])
@@ -144,6 +148,9 @@ class SideBySide:
             row_err = (np.max(np.abs(zg[b][:n_b] - zr), axis=-1) if check_logits
                        else rtol * np.max(np.abs(zr), axis=-1))
             ok = gap > np.maximum(1e-2, 2.0 * row_err)
+            band = (gap > 1e-2) & ~ok
+            rep["ids_band"] += int(band.sum())
+            rep["ids_band_equal"] += int((dg[b][:n_b][band] == od[k][:n_b][band]).sum())
             rep["ids_compared"] += int(ok.sum())
             rep["ids_equal"] += int((dg[b][:n_b][ok] == od[k][:n_b][ok]).sum())
             assert np.array_equal(dg[b][:n_b][ok], od[k][:n_b][ok]), f"seq {b} it {it}: draft ids differ where gap > 1e-2"
@@ -189,6 +196,9 @@ class SideBySide:
         st = self.gpu.query_state()
         assert np.all(st["kv_len"] == st["ctx_len"])
         self.report.append(rep)
+        print(f"[parity] {s.name} it {it}: ids compared {rep['ids_compared']} (equal {rep['ids_equal']}), "
+              f"excluded band (1e-2, 2 err] {rep['ids_band']} (equal {rep['ids_band_equal']}), "
+              f"max rel {rep['max_rel']:.3e}")
         path = os.environ.get("DFLASH_PARITY_REPORT")
         if path:
             with open(path, "a") as fh:

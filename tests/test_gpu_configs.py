@@ -52,40 +52,53 @@ def test_llama31_8b_batch8_sampled():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("K", [128, 1024])
+_KSWEEP_W = {}
+
+
+@pytest.mark.parametrize("K", [16, 32, 64, 128, 256, 1024])
 def test_qwen3_4b_k_sweep(K):
-    """The K sweep at context 4096: one draft -> verify -> append iteration with
-    K = 128 (one token tile) and K = 1024 (five token tiles per projection)."""
+    """The K sweep at context 4096, every block length of the workload: two
+    draft -> verify -> append iterations each, from K = 16 (split-operand token
+    tiles of 24 rows) through K = 128 (one token tile of a split operand per
+    CTA pair), K = 256 (fp16 operands) to K = 1024 (six token tiles per
+    projection).  The weights are drawn once for all K."""
     torch = _cuda()
     s = CONFIGS["qwen3_4b_ksweep"].with_(K=K)
-    Wn = make_weights(s)
+    if not _KSWEEP_W:
+        Wn = make_weights(s)
+        _KSWEEP_W["w"] = (Wn, upload_weights(Wn))
+    Wn, Wd = _KSWEEP_W["w"]
     ctx = context_lengths(s)
-    sb = SideBySide(s, Wn, upload_weights(Wn), K=K, ctx=ctx, iterations=2, kv_pool_tokens=_pool(s, ctx, 2, s.K_max),
+    sb = SideBySide(s, Wn, Wd, K=K, ctx=ctx, iterations=2, kv_pool_tokens=_pool(s, ctx, 2, s.K_max),
                     oracle_dtype=np.float32)
     sb.prefill_chunked([4242])
     for it in range(2):
         rep = sb.step(it, 2e-2)
         assert rep["ids_compared"] >= 3
     del sb
+    if K == 1024:
+        _KSWEEP_W.clear()
     torch.cuda.empty_cache()
 
 
 def test_serving_batch64_32_iterations_sampled():
     """Serving-shaped batch: 8 draft layers, 64 sequences with contexts
     log-uniform in [128, 16384], K = 16, 32 draft -> verify -> append
-    iterations (capacities grow by powers of two on the way); the shortest and
-    the longest context follow the oracle."""
+    iterations (capacities grow by powers of two on the way); the shortest,
+    the longest and the two median contexts follow the oracle, with logits
+    checked every fourth iteration and on the last."""
     torch = _cuda()
     s = CONFIGS["qwen3_4b_serving"]
     ctx = context_lengths(s)
-    oseqs = [int(np.argmin(ctx)), int(np.argmax(ctx))]
+    order = np.argsort(ctx)
+    oseqs = sorted({int(order[0]), int(order[-1]), int(order[len(order) // 2 - 1]), int(order[len(order) // 2])})
     Wn = make_weights(s)
     iters = s.iterations
     sb = SideBySide(s, Wn, upload_weights(Wn), K=s.K, ctx=ctx, oracle_seqs=oseqs, iterations=iters,
                     kv_pool_tokens=_pool(s, ctx, iters, s.K), oracle_dtype=np.float32)
     sb.prefill_chunked(list(range(1, s.batch + 1)), chunk=512)
     for it in range(iters):
-        sb.step(it, 2e-2, check_logits=it % 8 == 0 or it == iters - 1)
+        sb.step(it, 2e-2, check_logits=it % 4 == 0 or it == iters - 1)
     st = sb.gpu.query_state()
     assert np.all(st["ctx_len"] >= ctx + iters)          # every iteration commits the anchor at least
     assert np.all(st["capacity"] >= st["ctx_len"] + s.K + 1)
