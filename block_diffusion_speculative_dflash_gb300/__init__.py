@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     DflashError,
     DrafterConfig,
     EXPORTS,
+    inject_alloc_failure,
     load_library,
     plant_targets,
     ptr,

@@ -23,13 +23,15 @@ CONDITIONING = {"kv": 0, "input": 1, "none": 2}   # dflash_conditioning
 STATUS = {0: "DFLASH_OK", 1: "DFLASH_ERR_INVALID", 2: "DFLASH_ERR_OOM", 3: "DFLASH_ERR_CAPACITY",
           4: "DFLASH_ERR_CUDA", 5: "DFLASH_ERR_DEVICE_FLAG", 6: "DFLASH_ERR_UNSUPPORTED"}
 FLAG_BAD_TOKEN, FLAG_NOT_CONSUMED, FLAG_CAPACITY, FLAG_WAIT_TIMEOUT, FLAG_BAD_ROWS, FLAG_BAD_K = 1, 2, 4, 8, 16, 32
+FLAG_F16_RANGE = 64
 
 EXPORTS = ("dflash_create", "dflash_destroy", "dflash_reserve", "dflash_ctx_append", "dflash_draft_block",
            "dflash_verify_accept", "dflash_query_state", "dflash_last_error", "dflash_plant_targets",
            "dflash_trace_enable", "dflash_trace_read", "dflash_launch_count", "dflash_read_kv",
            "dflash_draft_block_noalloc", "dflash_reserve_headroom", "dflash_draft_block_k",
            "dflash_target_create", "dflash_target_destroy", "dflash_target_forward", "dflash_target_commit",
-           "dflash_target_query", "dflash_graph_replays")
+           "dflash_target_query", "dflash_graph_replays", "dflash_set_wait_limit", "dflash_selftest_wait",
+           "dflash_inject_alloc_failure", "dflash_check_guards")
 TRACE_GEMM, TRACE_APPEND, TRACE_DRAFT, TRACE_VERIFY, TRACE_ENGINE = 0, 1, 2, 3, 4
 
 
@@ -104,9 +106,14 @@ def load_library(build_if_needed: bool = True) -> ctypes.CDLL:
     lib.dflash_target_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp]
     lib.dflash_target_commit.argtypes = [vp, vp, vp]
     lib.dflash_target_query.argtypes = [vp, vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.dflash_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
+    lib.dflash_selftest_wait.argtypes = [vp, vp]
+    lib.dflash_inject_alloc_failure.argtypes = [ctypes.c_int64]
+    lib.dflash_check_guards.argtypes = [vp, vp]
     for name in EXPORTS:
-        if name != "dflash_last_error":
+        if name not in ("dflash_last_error", "dflash_inject_alloc_failure"):
             getattr(lib, name).restype = ctypes.c_int
+    lib.dflash_inject_alloc_failure.restype = ctypes.c_int64
     _lib = lib
     return lib
 
@@ -281,6 +288,19 @@ class DFlashDrafter:
         _check(self.lib.dflash_graph_replays(self.handle, ctypes.byref(v)))
         return int(v.value)
 
+    # -- failure detection ----------------------------------------------------
+    def set_wait_limit(self, limit_ns: int) -> None:
+        """Time limit of every bounded device wait of this context (0: the 2 s default)."""
+        _check(self.lib.dflash_set_wait_limit(self.handle, int(limit_ns)))
+
+    def selftest_wait(self, stream=None) -> None:
+        """One kernel whose wait nothing ends: it runs out and latches FLAG_WAIT_TIMEOUT."""
+        _check(self.lib.dflash_selftest_wait(self.handle, _stream(stream)))
+
+    def check_guards(self, stream=None) -> None:
+        """Raise DflashError if a guard band around the KV arena was written."""
+        _check(self.lib.dflash_check_guards(self.handle, _stream(stream)))
+
     def close(self) -> None:
         if getattr(self, "handle", None):
             self.lib.dflash_destroy(self.handle)
@@ -291,6 +311,12 @@ class DFlashDrafter:
             self.close()
         except Exception:
             pass
+
+
+def inject_alloc_failure(after: int) -> int:
+    """Make the after-th next device allocation of the library fail once (after < 0: off).
+    Returns the previous setting."""
+    return int(load_library().dflash_inject_alloc_failure(int(after)))
 
 
 def plant_targets(draft_ids, accept_len_plan, fill, batch: int, K: int, vocab: int, target_ids,
@@ -376,6 +402,19 @@ class DFlashTarget:
         flags = ctypes.c_uint32(0)
         _check(self.lib.dflash_target_query(self.handle, _stream(stream), ptr(ln), ctypes.byref(flags)))
         return ln
+
+    # -- failure detection ----------------------------------------------------
+    def set_wait_limit(self, limit_ns: int) -> None:
+        """Time limit of every bounded device wait of this context (0: the 2 s default)."""
+        _check(self.lib.dflash_set_wait_limit(self.handle, int(limit_ns)))
+
+    def selftest_wait(self, stream=None) -> None:
+        """One kernel whose wait nothing ends: it runs out and latches FLAG_WAIT_TIMEOUT."""
+        _check(self.lib.dflash_selftest_wait(self.handle, _stream(stream)))
+
+    def check_guards(self, stream=None) -> None:
+        """Raise DflashError if a guard band around the KV arena was written."""
+        _check(self.lib.dflash_check_guards(self.handle, _stream(stream)))
 
     def close(self) -> None:
         if getattr(self, "handle", None):

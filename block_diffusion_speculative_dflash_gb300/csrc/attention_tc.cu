@@ -226,6 +226,8 @@ __global__ void __launch_bounds__(288, 1) attn_tc_kernel(const __grid_constant__
 #pragma unroll
         for (int dt = 0; dt < 16; ++dt) {   // split bf16: hi plane, lo plane o_plane further
           if (p.o_plane == kF16Plane) {     // or one fp16 plane
+            check_f16(o[dt][2 * hf] * inv, p.flags);
+            check_f16(o[dt][2 * hf + 1] * inv, p.flags);
             *reinterpret_cast<__half2*>(orow + dt * 8 + 2 * q4) =
                 __floats2half2_rn(o[dt][2 * hf] * inv, o[dt][2 * hf + 1] * inv);
             continue;
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(288, 1) attn_tc_kernel(const __grid_constant__
           }
           const int gq = row / p.R, j = row % p.R;
           __nv_bfloat16* od = p.o + (size_t)(b * p.R + j) * qd + (size_t)(hk * p.G + gq) * 128 + d;
-          put_op(wsum > 0.f ? acc / wsum : 0.f, od, p.o_plane);
+          put_op(wsum > 0.f ? acc / wsum : 0.f, od, p.o_plane, p.flags);
         }
       }
       __syncthreads();
@@ -324,7 +326,8 @@ constexpr int kMergeBatch = 32;   // = warp size: lane d holds split d's lse
 __global__ void __launch_bounds__(128) attn_merge_dim_kernel(const float* __restrict__ part_o,
                                                              const float* __restrict__ part_lse, int n_kv, int S,
                                                              int rows, int rows_pad, int R, int G, int n_q,
-                                                             __nv_bfloat16* __restrict__ o, size_t o_plane) {
+                                                             __nv_bfloat16* __restrict__ o, size_t o_plane,
+                                                             uint32_t* flags) {
   pdl_trigger();
   pdl_wait();
   __shared__ float w_s[kMergeBatch];
@@ -373,7 +376,7 @@ __global__ void __launch_bounds__(128) attn_merge_dim_kernel(const float* __rest
   }
   const int gq = r / R, j = r % R;
   __nv_bfloat16* od = o + (size_t)(b * R + j) * n_q * 128 + (size_t)(hk * G + gq) * 128 + d;
-  put_op(wsum > 0.f ? acc / wsum : 0.f, od, o_plane);
+  put_op(wsum > 0.f ? acc / wsum : 0.f, od, o_plane, flags);
 }
 
 // o = sum_s w_s o_s / sum_s w_s with w_s = 2^(lse_s - max lse), sums in split
@@ -388,7 +391,7 @@ __global__ void __launch_bounds__(32 * kMergeRows) attn_merge_kernel(const float
                                                                     const float* __restrict__ part_lse, int n_kv,
                                                                     int S, int rows, int rows_pad, int R, int G,
                                                                     int n_q, __nv_bfloat16* __restrict__ o,
-                                                                    size_t o_plane) {
+                                                                    size_t o_plane, uint32_t* flags) {
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
@@ -431,6 +434,8 @@ __global__ void __launch_bounds__(32 * kMergeRows) attn_merge_kernel(const float
   const int gq = r / R, j = r % R;
   __nv_bfloat16* od = o + (size_t)(b * R + j) * n_q * 128 + (size_t)(hk * G + gq) * 128 + 4 * lane;
   if (o_plane == kF16Plane) {   // one fp16 plane
+#pragma unroll
+    for (int i = 0; i < 4; ++i) check_f16(y[i], flags);
     const __half2 h01 = __floats2half2_rn(y[0], y[1]), h23 = __floats2half2_rn(y[2], y[3]);
     *reinterpret_cast<uint2*>(od) =
         make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
@@ -466,7 +471,8 @@ int attn_tc_resident_ctas(int n_consumer_warps) {
 }
 
 cudaError_t launch_attn_merge(const float* part_o, const float* part_lse, int n_kv, int S, int rows, int rows_pad,
-                              int R, int G, int n_q, __nv_bfloat16* o, size_t o_plane, int B, cudaStream_t s) {
+                              int R, int G, int n_q, __nv_bfloat16* o, size_t o_plane, int B, cudaStream_t s,
+                              uint32_t* flags) {
   // rows per CTA: up to kMergeRows while the grid still gives every SM about two CTAs
   static int n_sm = 0;
   if (n_sm == 0) {
@@ -482,17 +488,20 @@ cudaError_t launch_attn_merge(const float* part_o, const float* part_lse, int n_
   }
   if (mode == 1 || (mode == 0 && total < 8 * 2 * (int64_t)n_sm)) {
     launch_k(attn_merge_dim_kernel, dim3(rows, n_kv, B), dim3(128), 0, s, part_o, part_lse, n_kv, S, rows, rows_pad, R,
-             G, n_q, o, o_plane);
+             G, n_q, o, o_plane, flags);
     return cudaGetLastError();
   }
   const int rpc = (int)std::max<int64_t>(1, std::min<int64_t>(kMergeRows, total / (2 * (int64_t)n_sm)));
   const dim3 grid((rows + rpc - 1) / rpc, n_kv, B), block(32 * rpc);
   if (S <= 4)
-    launch_k(attn_merge_kernel<4>, grid, block, 0, s, part_o, part_lse, n_kv, S, rows, rows_pad, R, G, n_q, o, o_plane);
+    launch_k(attn_merge_kernel<4>, grid, block, 0, s, part_o, part_lse, n_kv, S, rows, rows_pad, R, G, n_q, o, o_plane,
+             flags);
   else if (S <= 16)
-    launch_k(attn_merge_kernel<16>, grid, block, 0, s, part_o, part_lse, n_kv, S, rows, rows_pad, R, G, n_q, o, o_plane);
+    launch_k(attn_merge_kernel<16>, grid, block, 0, s, part_o, part_lse, n_kv, S, rows, rows_pad, R, G, n_q, o, o_plane,
+             flags);
   else
-    launch_k(attn_merge_kernel<32>, grid, block, 0, s, part_o, part_lse, n_kv, S, rows, rows_pad, R, G, n_q, o, o_plane);
+    launch_k(attn_merge_kernel<32>, grid, block, 0, s, part_o, part_lse, n_kv, S, rows, rows_pad, R, G, n_q, o, o_plane,
+             flags);
   return cudaGetLastError();
 }
 
@@ -509,7 +518,7 @@ cudaError_t launch_attention_tc(const AttnTcParams& p, int n_consumer_warps, int
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.n_splits == 1 || p.coop_merge) return e;
   return launch_attn_merge(p.part_o, p.part_lse, p.n_kv, p.n_splits, p.rows, p.rows_pad, p.R, p.G, p.n_q, p.o, p.o_plane,
-                           B, s);
+                           B, s, p.flags);
 }
 
 }  // namespace dfl

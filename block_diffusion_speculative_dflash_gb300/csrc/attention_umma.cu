@@ -393,6 +393,8 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
               uint32_t wh[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
+                check_f16(o16[2 * i] * inv, p.flags);
+                check_f16(o16[2 * i + 1] * inv, p.flags);
                 const __half2 v = __floats2half2_rn(o16[2 * i] * inv, o16[2 * i + 1] * inv);
                 wh[i] = *reinterpret_cast<const uint32_t*>(&v);
               }

@@ -120,9 +120,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Every spin-wait in these kernels gives up after this long, latches
-// DFLASH_FLAG_WAIT_TIMEOUT and lets the kernel unwind.
+// Every spin-wait in these kernels gives up after a time limit, latches
+// DFLASH_FLAG_WAIT_TIMEOUT and lets the kernel unwind.  The limit is the
+// context's (dflash_set_wait_limit): a 64-bit count of nanoseconds kept next to
+// its device flag word, at flags + 2 (zero: this default).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+__device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t* gflags) {
+  if (gflags == nullptr) return kWaitLimitNs;
+  const uint64_t v = *reinterpret_cast<const volatile uint64_t*>(gflags + 2);
+  return v != 0 ? v : kWaitLimitNs;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -173,7 +180,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if ((it & 255u) == 0u) {
       if (abort != nullptr && *abort) return false;
       if (gflags != nullptr && (*(const volatile uint32_t*)gflags & DFLASH_FLAG_WAIT_TIMEOUT)) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+      if (globaltimer_ns() - t0 > wait_limit_ns(gflags)) return false;
     }
   }
 }
@@ -253,13 +260,21 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16* hi, __nv_bflo
   *lo = __float2bfloat16_rn(x - __bfloat162float(h));
 }
 
+// fp16 operands hold |x| <= 65504: a value outside (or NaN) latches
+// DFLASH_FLAG_F16_RANGE, so the silent inf of the conversion is reported.
+__device__ __forceinline__ void check_f16(float x, uint32_t* flags) {
+  if (!(fabsf(x) <= 65504.0f)) set_flag(flags, DFLASH_FLAG_F16_RANGE);
+}
+
 // A token operand written as one fp16 plane instead (11 significant bits, one
 // MMA against fp16 copies of the weights): the lo-plane offset kF16Plane says so.
-__device__ __forceinline__ void put_op(float x, __nv_bfloat16* hi, size_t plane) {
-  if (plane == kF16Plane)
+__device__ __forceinline__ void put_op(float x, __nv_bfloat16* hi, size_t plane, uint32_t* flags) {
+  if (plane == kF16Plane) {
+    check_f16(x, flags);
     *reinterpret_cast<__half*>(hi) = __float2half_rn(x);
-  else
+  } else {
     split_bf16(x, hi, hi + plane);
+  }
 }
 
 // ---------------------------------------------------------------- tcgen05

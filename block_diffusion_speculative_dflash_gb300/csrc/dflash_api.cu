@@ -61,6 +61,17 @@ int fail(int code, const char* fmt, ...) {
     if (r_ != DFLASH_OK) return r_; \
   } while (0)
 
+// Allocation-failure injection (dflash_inject_alloc_failure): while >= 0, the
+// count of device allocations still to succeed before one fails.
+std::atomic<int64_t> g_alloc_fail_after{-1};
+bool injected_alloc_failure() {
+  int64_t v = g_alloc_fail_after.load();
+  while (v >= 0) {
+    if (g_alloc_fail_after.compare_exchange_weak(v, v - 1)) return v == 0;
+  }
+  return false;
+}
+
 int64_t next_pow2(int64_t v) {
   int64_t p = 1;
   while (p < v) p <<= 1;
@@ -225,6 +236,10 @@ constexpr size_t kCounters = 1u << 16;   // arrival counters of the fused GEMM e
 
 }  // namespace
 
+// Guard bands around the KV arena: bytes of kGuardByte on either side.
+constexpr size_t kGuardBytes = 4096;
+constexpr int kGuardByte = 0xA5;
+
 struct dflash_ctx {
   dflash_config cfg{};
   dflash_weights w{};
@@ -268,8 +283,10 @@ struct dflash_ctx {
   uint64_t* d_rope = nullptr;          // RoPE frequencies in turns, 0.64 fixed point
   SeqState st{};
 
-  // KV arena
+  // KV arena (inside arena_raw, between two guard bands of kGuardBytes)
   void* arena = nullptr;
+  void* arena_raw = nullptr;
+  size_t arena_bytes = 0;
   Buddy buddy;
   std::vector<int64_t> seg_tok, cap, ub_ctx, ub_kv;
   KvArena kv{};
@@ -400,7 +417,7 @@ int grow_buffer(void** p, size_t* cap, size_t bytes, cudaStream_t s, const char*
   *p = nullptr;
   *cap = 0;
   g_grow_epoch.fetch_add(1);
-  if (cudaMallocAsync(p, bytes, s) != cudaSuccess) {
+  if (injected_alloc_failure() || cudaMallocAsync(p, bytes, s) != cudaSuccess) {
     cudaGetLastError();
     *p = nullptr;
     return fail(DFLASH_ERR_OOM, "allocation of %zu bytes for %s failed", bytes, what);
@@ -881,7 +898,7 @@ int run_attention_umma(dflash_ctx* c, const void* qb, void* ob, int l, int R, cu
   c->launches += 1;
   if (p.n_splits > 1) {
     CK(launch_attn_merge(p.part_o, p.part_lse, p.n_kv, p.n_splits, p.G * R, p.rows_pad, R, p.G, p.n_q,
-                         p.o, p.o_plane, c->B, s));
+                         p.o, p.o_plane, c->B, s, c->d_flags));
     c->launches += 1;
   }
   return DFLASH_OK;
@@ -1193,7 +1210,7 @@ int engine_program(dflash_ctx* c, int K, bool lm_only, cudaStream_t s, dflash_ct
   if (pr->ctas_per_sm == 1) pr->stages = engine_stages_for(BN, XP, pr->scratch, 1);
   pr->nacc = std::min(4, (512 / pr->ctas_per_sm) / (XP * BN));   // accumulators of XP * BN TMEM columns
   const size_t attn_floats = a_splits > 1 ? (size_t)B * n_kv * a_splits * rows_pad * 129 : 0;
-  if (cudaMalloc(&pr->ws0, std::max<size_t>(1, ws_floats) * sizeof(float)) != cudaSuccess ||
+  if (injected_alloc_failure() || cudaMalloc(&pr->ws0, std::max<size_t>(1, ws_floats) * sizeof(float)) != cudaSuccess ||
       cudaMalloc(&pr->ws1, std::max<size_t>(1, ws_floats) * sizeof(float)) != cudaSuccess ||
       (attn_floats && cudaMalloc(&pr->attn, attn_floats * sizeof(float)) != cudaSuccess)) {
     cudaGetLastError();
@@ -1255,7 +1272,7 @@ bool ensure_w16(dflash_ctx* c, cudaStream_t s) {
     for (size_t e : sz) n += e;
   const size_t bad_off = (2 * n + 15) & ~(size_t)15;
   char* buf = nullptr;
-  if (cudaMalloc(&buf, bad_off + 16) != cudaSuccess) {
+  if (injected_alloc_failure() || cudaMalloc(&buf, bad_off + 16) != cudaSuccess) {
     cudaGetLastError();
     c->w16_failed = true;
     return false;
@@ -1748,7 +1765,7 @@ void free_ctx(dflash_ctx* c) {
     delete pr;
   }
   if (c->d_phase_cnt) cudaFree(c->d_phase_cnt);
-  void* ptrs[] = {c->d_i32, c->d_kv_base, c->d_flags, c->d_draft, c->d_targets, c->d_rope, c->arena, c->h,
+  void* ptrs[] = {c->d_i32, c->d_kv_base, c->d_flags, c->d_draft, c->d_targets, c->d_rope, c->arena_raw, c->h,
                   c->xn, c->qb, c->ob, c->ab, c->xf, c->ws, c->stage, c->ub, c->attn_ws, c->d_keys,
                   c->d_counters, c->d_ss, c->ybuf, c->d_ss_ctx, c->d_ulast, c->d_seq_order, c->w16};
   for (void* p : ptrs)
@@ -1898,7 +1915,7 @@ static int create_impl(const dflash_config* cfg, const dflash_weights* w, int32_
     return code;
   };
   auto dalloc = [&](void** p, size_t bytes) -> bool {
-    if (cudaMalloc(p, bytes) != cudaSuccess) {
+    if (injected_alloc_failure() || cudaMalloc(p, bytes) != cudaSuccess) {
       cudaGetLastError();
       *p = nullptr;
       return false;
@@ -2017,11 +2034,18 @@ static int create_impl(const dflash_config* cfg, const dflash_weights* w, int32_
   if (c->bf16 && arena_rows >= ((int64_t)1 << 31))
     return bail(fail(DFLASH_ERR_UNSUPPORTED, "KV arena of %lld rows exceeds the 2^31 rows a tensor map addresses",
                      (long long)arena_rows));
-  if (!dalloc(&c->arena, arena_bytes))
+  // the arena sits between two guard bands of a known byte pattern
+  // (dflash_check_guards): a write past either end of it shows there
+  if (!dalloc(&c->arena_raw, arena_bytes + 2 * kGuardBytes))
     return bail(fail(DFLASH_ERR_OOM, "KV arena of %zu bytes (%lld slots) failed", arena_bytes,
                      (long long)c->buddy.pool()));
+  c->arena = static_cast<char*>(c->arena_raw) + kGuardBytes;
+  c->arena_bytes = arena_bytes;
   // zero once: every slot attention may touch (including masked tail slots of a tile) holds finite values
-  if (cudaMemset(c->arena, 0, arena_bytes) != cudaSuccess) return bail(fail(DFLASH_ERR_CUDA, "arena memset failed"));
+  if (cudaMemset(c->arena, 0, arena_bytes) != cudaSuccess ||
+      cudaMemset(c->arena_raw, kGuardByte, kGuardBytes) != cudaSuccess ||
+      cudaMemset(static_cast<char*>(c->arena) + arena_bytes, kGuardByte, kGuardBytes) != cudaSuccess)
+    return bail(fail(DFLASH_ERR_CUDA, "arena memset failed"));
   c->kv = KvArena{c->arena, c->nl, g.n_kv_heads, c->d};
   c->seg_tok.assign(B, 0);
   c->cap.assign(B, 0);
@@ -2363,6 +2387,48 @@ int dflash_launch_count(dflash_ctx* c, int64_t* launches) {
 int dflash_graph_replays(dflash_ctx* c, int64_t* replays) {
   if (!c || !replays) return fail(DFLASH_ERR_INVALID, "bad argument");
   *replays = c->replays;
+  return DFLASH_OK;
+}
+
+int dflash_set_wait_limit(dflash_ctx* c, uint64_t limit_ns) {
+  g_err.clear();
+  if (!c) return fail(DFLASH_ERR_INVALID, "null context");
+  // the limit sits next to the flag word: flags + 2 (8 bytes, 8-byte aligned)
+  if (cudaMemcpy(c->d_flags + 2, &limit_ns, sizeof(limit_ns), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DFLASH_ERR_CUDA, "wait-limit upload failed");
+  }
+  return DFLASH_OK;
+}
+
+int dflash_selftest_wait(dflash_ctx* c, void* stream) {
+  g_err.clear();
+  if (!c) return fail(DFLASH_ERR_INVALID, "null context");
+  CK(launch_wait_selftest(c->d_flags, reinterpret_cast<cudaStream_t>(stream)));
+  c->launches += 1;
+  return DFLASH_OK;
+}
+
+int64_t dflash_inject_alloc_failure(int64_t after) {
+  return g_alloc_fail_after.exchange(after < 0 ? -1 : after);
+}
+
+int dflash_check_guards(dflash_ctx* c, void* stream) {
+  g_err.clear();
+  if (!c) return fail(DFLASH_ERR_INVALID, "null context");
+  if (c->arena_raw == nullptr) return DFLASH_OK;
+  std::vector<unsigned char> g(2 * kGuardBytes);
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      cudaMemcpy(g.data(), c->arena_raw, kGuardBytes, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(g.data() + kGuardBytes, static_cast<char*>(c->arena) + c->arena_bytes, kGuardBytes,
+                 cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DFLASH_ERR_CUDA, "guard-band read failed");
+  }
+  for (size_t i = 0; i < g.size(); ++i)
+    if (g[i] != (unsigned char)kGuardByte)
+      return fail(DFLASH_ERR_DEVICE_FLAG, "KV arena guard band %s the arena overwritten at byte %zu",
+                  i < kGuardBytes ? "before" : "after", i < kGuardBytes ? i : i - kGuardBytes);
   return DFLASH_OK;
 }
 

@@ -116,7 +116,7 @@ __global__ void embed_norm_kernel(const T* __restrict__ E, const int32_t* __rest
   T* y = xn + (size_t)m * H;
   if constexpr (std::is_same<T, __nv_bfloat16>::value) {
     if (lo_plane) {   // split bf16: hi plane, then lo plane lo_plane elements further (kF16Plane: fp16)
-      for (int i = threadIdx.x; i < H; i += blockDim.x) put_op(out[i] * inv * ldf(gain + i), y + i, lo_plane);
+      for (int i = threadIdx.x; i < H; i += blockDim.x) put_op(out[i] * inv * ldf(gain + i), y + i, lo_plane, flags);
       return;
     }
   }
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kEmbThreads) embed_norm_vec_kernel(
     if constexpr (std::is_same<T, __nv_bfloat16>::value) {
       if (lo_plane) {   // split bf16: hi plane, then lo plane lo_plane elements further
 #pragma unroll
-        for (int q = 0; q < VEC; ++q) put_op(f[q] * inv * g[q], y + (size_t)i * VEC + q, lo_plane);
+        for (int q = 0; q < VEC; ++q) put_op(f[q] * inv * g[q], y + (size_t)i * VEC + q, lo_plane, flags);
         continue;
       }
     }
@@ -881,6 +881,25 @@ void launch_lm_argmax(const float* ws, int splits, int M, int V, int R, const fl
 void launch_argmax(float* ws, int splits, int rows, int V, int32_t* ids, cudaStream_t s) {
   launch_k(argmax_kernel, dim3(rows), dim3(512), 0, s, ws, splits, rows, V, ids);
 }
+// Failure-detection self-test: one wait that can only end by running out of
+// time -- an mbarrier nothing ever arrives at.  The bounded wait gives up after
+// the context's limit, the kernel latches DFLASH_FLAG_WAIT_TIMEOUT and returns,
+// and the context stays usable.
+__global__ void wait_selftest_kernel(uint32_t* flags) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0u, nullptr, flags)) set_flag(flags, DFLASH_FLAG_WAIT_TIMEOUT);
+}
+
+cudaError_t launch_wait_selftest(uint32_t* flags, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(flags);
+  return cudaGetLastError();
+}
+
 void launch_accept(const int32_t* drafts, const int32_t* targets, int B, int K, int V, SeqState st,
                    int32_t* accept_len, int32_t* next_anchor, uint32_t* flags, cudaStream_t s) {
   launch_k(accept_kernel, dim3((B + 127) / 128), dim3(128), 0, s, drafts, targets, B, K, V, st, accept_len, next_anchor, flags);

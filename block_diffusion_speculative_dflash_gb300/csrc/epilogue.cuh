@@ -293,7 +293,7 @@ __device__ bool wait_count(const unsigned int* cnt, unsigned int expected, const
     __nanosleep(64);
     if ((it & 63u) == 63u) {
       if (*(const volatile uint32_t*)gflags & DFLASH_FLAG_WAIT_TIMEOUT) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+      if (globaltimer_ns() - t0 > wait_limit_ns(gflags)) return false;
     }
   }
 }
@@ -496,7 +496,7 @@ __device__ void epi_resid(const EpiArgs& p, const Red& red, int r, int tile, int
           if (i < n) {
             if (p.h != nullptr) p.h[(size_t)t * p.N + gcol] = v;
             if (p.xn_out != nullptr)
-              put_op(v * gain, p.xn_out + (size_t)t * p.N + gcol, p.op16 ? kF16Plane : (size_t)p.M * p.N);
+              put_op(v * gain, p.xn_out + (size_t)t * p.N + gcol, p.op16 ? kF16Plane : (size_t)p.M * p.N, p.flags);
           }
           sq[i] = v * v;   // slots past n are summed but never stored
         }
@@ -528,7 +528,7 @@ __device__ void epi_resid(const EpiArgs& p, const Red& red, int r, int tile, int
           const float v = add ? acc[i] + hv[i] : acc[i];
           if (p.h != nullptr) p.h[(size_t)t * p.N + gcol] = v;
           if (p.xn_out != nullptr)
-            put_op(v * gain, p.xn_out + (size_t)t * p.N + gcol, p.op16 ? kF16Plane : (size_t)p.M * p.N);
+            put_op(v * gain, p.xn_out + (size_t)t * p.N + gcol, p.op16 ? kF16Plane : (size_t)p.M * p.N, p.flags);
           const float sq = warp_sum(v * v);
           if (lane == 0) sm[warp * kEpiChunk + i0 + i] = sq;
         }
@@ -666,7 +666,7 @@ __device__ void epi_silu(const EpiArgs& p, const Red& red, int r, int pair, int 
         if (i >= n) break;
         const float gs = g[i] * sc[t0 + i - n0], us = u[i] * sc[t0 + i - n0];
         put_op(gs / (1.0f + expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
-               p.op16 ? kF16Plane : (size_t)p.M * I);
+               p.op16 ? kF16Plane : (size_t)p.M * I, p.flags);
       }
     }
     return;
@@ -680,7 +680,7 @@ __device__ void epi_silu(const EpiArgs& p, const Red& red, int r, int pair, int 
       if (i >= n) break;
       const float gs = g[i] * sc[t0 + i - n0], us = u[i] * sc[t0 + i - n0];
       put_op(gs / (1.0f + expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
-             p.op16 ? kF16Plane : (size_t)p.M * I);
+             p.op16 ? kF16Plane : (size_t)p.M * I, p.flags);
     }
   }
 }

@@ -290,7 +290,8 @@ struct AttnUParams {
 size_t attn_umma_smem_bytes();
 cudaError_t launch_attention_umma(const AttnUParams& p, int B, cudaStream_t s);
 cudaError_t launch_attn_merge(const float* part_o, const float* part_lse, int n_kv, int S, int rows, int rows_pad,
-                              int R, int G, int n_q, __nv_bfloat16* o, size_t o_plane, int B, cudaStream_t s);
+                              int R, int G, int n_q, __nv_bfloat16* o, size_t o_plane, int B, cudaStream_t s,
+                              uint32_t* flags);
 size_t attn_tc_smem_bytes();
 int attn_tc_resident_ctas(int n_consumer_warps);   // CTAs of attn_tc_kernel resident per SM
 cudaError_t launch_attention_tc(const AttnTcParams& p, int n_consumer_warps, int B, cudaStream_t s);
@@ -359,6 +360,10 @@ void launch_attention(const T* q, SeqState st, KvArena kv, int layer, int B, int
 // target forward: greedy ids are per row; features of a layer copied out; commit
 void launch_feat_copy(const float* h, int M, int H, int n_feat, int fi, __nv_bfloat16* feats, cudaStream_t s);
 void launch_target_commit(const int32_t* keep, SeqState st, int B, uint32_t* flags, cudaStream_t s);
+
+// The failure-detection self-test kernel (one wait that nothing ends; it runs
+// out after the context's wait limit and latches DFLASH_FLAG_WAIT_TIMEOUT).
+cudaError_t launch_wait_selftest(uint32_t* flags, cudaStream_t s);
 
 // bf16 -> fp16 copy of n elements; *bad |= 1 where a value is outside fp16's range.
 cudaError_t launch_bf16_to_f16(const __nv_bfloat16* x, void* y, size_t n, uint32_t* bad, cudaStream_t s);

@@ -77,6 +77,8 @@ typedef enum { DFLASH_COND_KV = 0, DFLASH_COND_INPUT = 1, DFLASH_COND_NONE = 2 }
 #define DFLASH_FLAG_WAIT_TIMEOUT   0x8u  /* a bounded mbarrier wait ran out: kernel returned */
 #define DFLASH_FLAG_BAD_ROWS       0x10u /* append row count outside [0, rows_max]: clamped */
 #define DFLASH_FLAG_BAD_K          0x20u /* per-sequence K outside [1, K]: clamped */
+#define DFLASH_FLAG_F16_RANGE      0x40u /* an fp16 GEMM operand (drafts of > 128 rows) outside
+                                            +-65504 or NaN: the value was stored as fp16 inf/NaN */
 
 /* Drafter shape.  All matrix widths must be multiples of 64; head_dim 64 or 128;
    n_q_heads a multiple of n_kv_heads. */
@@ -350,6 +352,38 @@ int dflash_target_commit(dflash_target* t, const int32_t* keep, void* stream);
 /* Synchronise `stream`; len: host int32 [batch] of committed lengths (or NULL);
  * returns DFLASH_ERR_DEVICE_FLAG with the latched bits in *device_flags. */
 int dflash_target_query(dflash_target* t, void* stream, int32_t* len, uint32_t* device_flags);
+
+/* ---------------------------------------------------------------- failure detection
+ * (the survey's auxiliary subsystem: bounded device waits, allocation failures,
+ * KV arena guard bands).  The pages have no counterpart for these: they are
+ * the library's own error-handling surface.
+ *
+ * Time limit of every bounded wait in this context's kernels (mbarrier and
+ * cross-CTA counter waits), in nanoseconds; 0 restores the default of 2 s.  A
+ * wait that runs out latches DFLASH_FLAG_WAIT_TIMEOUT, its kernel unwinds
+ * (in-flight copies land, tensor memory is freed) and the context stays usable
+ * once dflash_query_state has returned the flag.  Synchronous; do not call it
+ * while a kernel of the context runs. */
+int dflash_set_wait_limit(dflash_ctx* ctx, uint64_t limit_ns);
+
+/* Self-test of the bounded waits: launches one kernel on `stream` whose single
+ * wait is on an mbarrier that nothing arrives at, so it can only end by running
+ * out of the context's wait limit; it then latches DFLASH_FLAG_WAIT_TIMEOUT
+ * (read it with dflash_query_state) and returns.  It holds one SM for the
+ * length of the limit: set a short one first. */
+int dflash_selftest_wait(dflash_ctx* ctx, void* stream);
+
+/* Allocation-failure injection (process-wide test hook): with after >= 0 the
+ * after-th next device allocation the library makes (0: the very next one)
+ * fails as if the device were out of memory, once -- the call that made it
+ * returns DFLASH_ERR_OOM and frees what it had taken; after < 0 disables it.
+ * Returns the previous setting (the allocations still to succeed, or -1). */
+int64_t dflash_inject_alloc_failure(int64_t after);
+
+/* Synchronise `stream` and check the guard bands of 4096 bytes of 0xA5 on both
+ * sides of the KV arena: DFLASH_OK, or DFLASH_ERR_DEVICE_FLAG naming the band
+ * and the first byte written where no kernel may write. */
+int dflash_check_guards(dflash_ctx* ctx, void* stream);
 
 #ifdef __cplusplus
 }

@@ -195,6 +195,7 @@ class SideBySide:
                 self.orc.ctx_append(i, f[b, :rows[b]])
         st = self.gpu.query_state()
         assert np.all(st["kv_len"] == st["ctx_len"])
+        self.gpu.check_guards()   # nothing wrote past either end of the KV arena
         self.report.append(rep)
         print(f"[parity] {s.name} it {it}: ids compared {rep['ids_compared']} (equal {rep['ids_equal']}), "
               f"excluded band (1e-2, 2 err] {rep['ids_band']} (equal {rep['ids_band_equal']}), "

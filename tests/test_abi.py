@@ -82,3 +82,18 @@ def test_invalid_arguments_return_status_without_device(lib):
 def test_build_is_sm103a_only():
     from block_diffusion_speculative_dflash_gb300 import _build
     assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_alloc_failure_injection_hook(lib):
+    """The host hook behind DFLASH_ERR_OOM injection: a process-wide counter,
+    set and read back without touching a device."""
+    from block_diffusion_speculative_dflash_gb300 import inject_alloc_failure
+    try:
+        assert inject_alloc_failure(-1) == -1      # off by default
+        assert inject_alloc_failure(5) == -1
+        assert inject_alloc_failure(2) == 5
+        assert inject_alloc_failure(-7) == 2       # any negative value turns it off
+        assert inject_alloc_failure(-1) == -1
+    finally:
+        inject_alloc_failure(-1)
+
