@@ -288,6 +288,81 @@ def target_verify_bench(args):
     print(json.dumps(line), flush=True)
 
 
+def k_sweep_bench(Wd, K_list, steps: int, warmup: int):
+    """Draft + accept step time against the block length at context 4096 (the
+    K-sweep workload), with the weights already on the device (the Qwen3-4B
+    shape; their values do not change a timing).  One drafter, a captured
+    draft + accept graph per K replayed between CUDA events, the context append
+    of the committed rows replayed between the timed spans."""
+    import torch
+    from block_diffusion_speculative_dflash_gb300 import DFlashDrafter, DrafterConfig, plant_targets
+    from synth import CONFIGS, context_lengths, draw_accept_lengths, make_target_fill
+    s = CONFIGS["qwen3_4b_ksweep"].with_(K_max=max(K_list))
+    B, Rm = s.batch, max(K_list) + 1
+    ctx = context_lengths(s)
+    T = len(K_list) * (steps + warmup + 2) + 4
+    pool = int(sum(1 << int(np.ceil(np.log2(max(64, int(c) + (T + 4) * Rm + Rm)))) for c in ctx)) * 2
+    dr = DFlashDrafter(DrafterConfig.from_shape(s, kv_pool_tokens=pool), Wd, B)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(2000 + s.seed)
+    f0 = torch.randn((B, int(ctx.max()), s.feat_dim), generator=gen, device="cuda").to(torch.bfloat16)
+    dr.ctx_append(f0, int(ctx.max()), rows=ctx.astype(np.int32))
+    del f0
+    dr.reserve_headroom((T + 4) * Rm + Rm)
+    stream = torch.cuda.current_stream()
+    out = {}
+    first = True
+    for K in K_list:
+        R = K + 1
+        L_tab = dev(draw_accept_lengths(s.with_(K=K), steps + warmup + 2, K))
+        fill_tab = dev(make_target_fill(s.with_(K=K), steps + warmup + 2, K))
+        ctr = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fstep = dev(feats_rows(s, [R] * B, R, "step"))
+        d_ids = torch.zeros((B, K), dtype=torch.int32, device="cuda")
+        g_ids = torch.zeros((B, R), dtype=torch.int32, device="cuda")
+        acc = torch.zeros(B, dtype=torch.int32, device="cuda")
+        nxt = torch.zeros(B, dtype=torch.int32, device="cuda")
+        rows = torch.zeros(B, dtype=torch.int32, device="cuda")
+
+        def draft_accept():
+            dr.draft_block(K, draft_ids=d_ids)
+            plant_targets(d_ids, L_tab, fill_tab, B, K, s.vocab, g_ids, step_counter=ctr, n_plans=steps + warmup + 2)
+            dr.verify_accept(g_ids, accept_len=acc, next_anchor=nxt)
+
+        def append():
+            torch.add(acc, 1, out=rows)
+            dr.ctx_append(fstep, R, rows=rows)
+
+        dr.draft_block(K, anchor_ids=dev(np.arange(1, B + 1, dtype=np.int32)) if first else None, draft_ids=d_ids)
+        first = False
+        plant_targets(d_ids, L_tab, fill_tab, B, K, s.vocab, g_ids, step_counter=ctr, n_plans=steps + warmup + 2)
+        dr.verify_accept(g_ids, accept_len=acc, next_anchor=nxt)
+        append()
+        torch.cuda.synchronize()
+        g_da, g_ap = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_da):
+            draft_accept()
+        with torch.cuda.graph(g_ap):
+            append()
+        for _ in range(warmup):
+            g_da.replay()
+            g_ap.replay()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for ea, eb in evs:
+            ea.record(stream)
+            g_da.replay()
+            eb.record(stream)
+            g_ap.replay()
+        torch.cuda.synchronize()
+        out[str(K)] = round(float(np.mean([ea.elapsed_time(eb) for ea, eb in evs])) * 1e3, 1)
+        del g_da, g_ap
+    dr.query_state()
+    dr.close()
+    return {"us_per_step": out, "context": int(ctx.max()), "steps": steps, "warmup": warmup,
+            "k128_over_k16": round(out["128"] / out["16"], 3) if "128" in out and "16" in out else None,
+            "what": "draft + accept step of the Qwen3-4B-shaped drafter at context 4096, per K (mask tokens)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -303,6 +378,8 @@ def main():
     ap.add_argument("--target-verify", action="store_true",
                     help="time the target-side verify forward against the block width instead")
     ap.add_argument("--target-r", default="1,2,9,17,33,65,129,257,513,1025")
+    ap.add_argument("--k-sweep", default="16,32,64,128",
+                    help="block lengths of the context-4096 K sweep reported beside the headline ('' to skip)")
     ap.add_argument("--conditioning", default="kv", choices=["kv", "input", "none"],
                     help="how the target context conditions the draft: K/V injection (the method), "
                          "input fusion or none (the ablation variants)")
@@ -575,6 +652,13 @@ def main():
                               "next anchors to pinned host memory (one synchronisation) -> append of the "
                               "accepted rows' features from pinned host memory; copies and the sync timed"}
         dr2.query_state()
+
+    # ---- the K sweep at context 4096 (the flatness of the step against K) -----------
+    if args.k_sweep and args.config == "qwen3_4b" and args.conditioning == "kv" and world == 1:
+        dr.close()
+        torch.cuda.synchronize()
+        out["k_sweep"] = k_sweep_bench(Wd, [int(k) for k in args.k_sweep.split(",")], steps=min(args.steps, 10),
+                                       warmup=3)
 
     # ---- CPU oracle baseline on a bounded sample (rank 0, N=1 only) -----------------
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

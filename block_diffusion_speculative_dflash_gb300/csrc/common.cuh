@@ -125,10 +125,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // context's (dflash_set_wait_limit): a 64-bit count of nanoseconds kept next to
 // its device flag word, at flags + 2 (zero: this default).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-__device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t* gflags) {
-  if (gflags == nullptr) return kWaitLimitNs;
-  const uint64_t v = *reinterpret_cast<const volatile uint64_t*>(gflags + 2);
-  return v != 0 ? v : kWaitLimitNs;
+// The flag word and the wait limit in one 16-byte load (the flags are 16-byte
+// aligned): a waiting thread checks both without an extra round trip.
+__device__ __forceinline__ void ld_flags_limit(const uint32_t* gflags, uint32_t* fl, uint64_t* limit) {
+  uint64_t a, b;
+  asm volatile("ld.volatile.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(gflags) : "memory");
+  *fl = (uint32_t)a;
+  *limit = b != 0 ? b : kWaitLimitNs;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -175,12 +178,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
                                           const uint32_t* gflags = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  uint64_t limit = kWaitLimitNs;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0u) {
       if (abort != nullptr && *abort) return false;
-      if (gflags != nullptr && (*(const volatile uint32_t*)gflags & DFLASH_FLAG_WAIT_TIMEOUT)) return false;
-      if (globaltimer_ns() - t0 > wait_limit_ns(gflags)) return false;
+      if (gflags != nullptr) {
+        uint32_t fl;
+        ld_flags_limit(gflags, &fl, &limit);
+        if (fl & DFLASH_FLAG_WAIT_TIMEOUT) return false;
+      }
+      if (globaltimer_ns() - t0 > limit) return false;
     }
   }
 }

@@ -292,8 +292,11 @@ __device__ bool wait_count(const unsigned int* cnt, unsigned int expected, const
     if (ld_acquire(cnt) >= expected) return true;
     __nanosleep(64);
     if ((it & 63u) == 63u) {
-      if (*(const volatile uint32_t*)gflags & DFLASH_FLAG_WAIT_TIMEOUT) return false;
-      if (globaltimer_ns() - t0 > wait_limit_ns(gflags)) return false;
+      uint32_t fl;
+      uint64_t limit;
+      ld_flags_limit(gflags, &fl, &limit);
+      if (fl & DFLASH_FLAG_WAIT_TIMEOUT) return false;
+      if (globaltimer_ns() - t0 > limit) return false;
     }
   }
 }
