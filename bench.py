@@ -566,12 +566,8 @@ def main():
     traffic = lm_traffic(s, K)
     da_gbs = draft_bytes / (ms_da / 1e3) / 1e9
     it_gbs = (draft_bytes + append_bytes) / (ms_it / 1e3) / 1e9
-    lm_kernel = ("engine_kernel, one-phase LM-head program (tcgen05 weight stream + fused greedy argmax)"
-                 if s.dtype == "bf16" and B * R <= 256 and os.environ.get("DFLASH_LM_ENGINE", "0") == "1"
-                 else "gemm_tc_kernel (tcgen05 weight stream, fp32 partial store) + lm_argmax_kernel"
-                 if s.dtype == "bf16" and B * R <= 256
-                 else "gemm_tc_kernel (tcgen05 weight stream + fused greedy argmax)" if s.dtype == "bf16"
-                 else "gemm_simt_kernel + argmax_kernel")
+    lm_kernel = ("gemm_tc_kernel (tcgen05 weight stream, fp32 partial store) + lm_argmax_kernel"
+                 if s.dtype == "bf16" else "gemm_simt_kernel + argmax_kernel")
 
     out = {
         "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world, "steps": args.steps,

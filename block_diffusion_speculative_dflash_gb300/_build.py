@@ -19,7 +19,7 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libdflash.so")
 
 SOURCES = ["dflash_api.cu", "gemm_tc.cu", "gemm_simt.cu", "elementwise.cu", "attention.cu", "attention_tc.cu",
-           "attention_umma.cu", "engine.cu", "noalloc.cu"]
+           "attention_umma.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -20,7 +20,6 @@
 
 #include "attn_mma.cuh"
 #include "common.cuh"
-#include "epilogue.cuh"
 #include "internal.h"
 
 namespace dfl {
@@ -258,64 +257,6 @@ __global__ void __launch_bounds__(288, 1) attn_tc_kernel(const __grid_constant__
     for (int t = max(0, issued - kStages); t < issued; ++t)
       (void)mbar_wait(&full[t % kStages], (uint32_t)(t / kStages) & 1u, nullptr);
   }
-  if (p.n_splits > 1 && p.coop_merge && !*abort_flag) {
-    // every CTA of the group publishes its partial (the barrier above ordered the
-    // consumer warps' stores before this release), waits for the others, and
-    // merges its slice of the group's rows: o = sum_s w_s o_s / sum_s w_s with
-    // w_s = 2^(lse_s - max lse), in split order
-    unsigned int* cnt = p.counters + 2 * ((b * p.n_kv + hk) * p.n_qtiles + qt);
-    volatile int* mflag = abort_flag + 1;
-    if (threadIdx.x == 0) {
-      red_release_add(cnt, 1u);
-      *mflag = wait_count(cnt, (unsigned)p.n_splits, p.flags) ? 1 : 0;
-      if (!*mflag) set_flag(p.flags, DFLASH_FLAG_WAIT_TIMEOUT);
-    }
-    __syncthreads();
-    if (*mflag) {
-      const int S = p.n_splits, qd = p.n_q * 128;
-      const int row_lo = qt * NW * 16, row_hi = min(p.rows, row_lo + NW * 16);
-      const int per = (row_hi - row_lo + S - 1) / S;
-      const int lo = min(row_hi, row_lo + split * per), hi = min(row_hi, lo + per);
-      const size_t base = (size_t)(b * p.n_kv + hk) * S * p.rows_pad;
-      float* lse_s = reinterpret_cast<float*>(tiles);   // the tile ring is idle now
-      const int n = (hi - lo) * S;
-      for (int i = threadIdx.x; i < n; i += blockDim.x)
-        lse_s[i] = __ldcg(p.part_lse + base + (size_t)(i % S) * p.rows_pad + lo + i / S);
-      __syncthreads();
-      for (int d = threadIdx.x; d < 128; d += blockDim.x) {
-        for (int row = lo; row < hi; ++row) {
-          const float* ls = lse_s + (row - lo) * S;
-          float mx = -INFINITY;
-          for (int sp = 0; sp < S; ++sp) mx = fmaxf(mx, ls[sp]);
-          float acc = 0.f, wsum = 0.f;
-          for (int s0 = 0; s0 < S; s0 += 8) {   // 8 unconditional loads in flight
-            float v[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              v[k] = __ldcg(p.part_o + (base + (size_t)min(s0 + k, S - 1) * p.rows_pad + row) * 128 + d);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              if (s0 + k >= S || ls[s0 + k] == -INFINITY) continue;
-              const float wt = exp2f(ls[s0 + k] - mx);
-              acc += wt * v[k];
-              wsum += wt;
-            }
-          }
-          const int gq = row / p.R, j = row % p.R;
-          __nv_bfloat16* od = p.o + (size_t)(b * p.R + j) * qd + (size_t)(hk * p.G + gq) * 128 + d;
-          put_op(wsum > 0.f ? acc / wsum : 0.f, od, p.o_plane, p.flags);
-        }
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        const unsigned int prev = atomicAdd(cnt + 1, 1u);
-        if (prev == (unsigned)S - 1) {   // every member is done: reset for the next launch
-          cnt[0] = 0u;
-          cnt[1] = 0u;
-        }
-      }
-    }
-  }
 }
 
 // The same merge with one CTA per row and thread d = output dimension d (four
@@ -455,21 +396,6 @@ __global__ void __launch_bounds__(32 * kMergeRows) attn_merge_kernel(const float
 
 size_t attn_tc_smem_bytes() { return 1024 + kStages * kStageBytes + 2 * kStages * 8 + 16; }
 
-int attn_tc_resident_ctas(int n_consumer_warps) {
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_tc_smem_bytes()) !=
-        cudaSuccess)
-      return 0;
-    configured = true;
-  }
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_tc_kernel, (n_consumer_warps + 1) * 32,
-                                                    attn_tc_smem_bytes()) != cudaSuccess)
-    return 0;
-  return n;
-}
-
 cudaError_t launch_attn_merge(const float* part_o, const float* part_lse, int n_kv, int S, int rows, int rows_pad,
                               int R, int G, int n_q, __nv_bfloat16* o, size_t o_plane, int B, cudaStream_t s,
                               uint32_t* flags) {
@@ -516,7 +442,7 @@ cudaError_t launch_attention_tc(const AttnTcParams& p, int n_consumer_warps, int
   dim3 grid(p.n_splits, p.n_kv * p.n_qtiles, B);
   launch_k(attn_tc_kernel, dim3(grid), dim3((n_consumer_warps + 1) * 32), smem, s, p);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || p.n_splits == 1 || p.coop_merge) return e;
+  if (e != cudaSuccess || p.n_splits == 1) return e;
   return launch_attn_merge(p.part_o, p.part_lse, p.n_kv, p.n_splits, p.rows, p.rows_pad, p.R, p.G, p.n_q, p.o, p.o_plane,
                            B, s, p.flags);
 }

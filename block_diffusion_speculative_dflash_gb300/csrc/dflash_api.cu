@@ -332,28 +332,8 @@ struct dflash_ctx {
 
   int last_K = 0;
 
-  // draft engine programs (one per K and attention split count); each owns its
-  // descriptors, tensor maps and workspaces, which never move once built, so
-  // a captured graph that launched one stays valid
-  struct EngProgram {
-    int K = 0, a_splits = 0, lm_only = 0, n_phases = 0, BN = 0, stages = 0, nacc = 0, x_planes = 2;
-    int ctas_per_sm = 1;
-    size_t scratch = 0;
-    EngPhase* d_phases = nullptr;
-    CUtensorMap* d_maps = nullptr;
-    float *ws0 = nullptr, *ws1 = nullptr, *attn = nullptr;
-    void* h_pinned = nullptr;   // staging of the upload (kept: a captured copy may replay it)
-  };
-  std::vector<EngProgram*> progs;
-  unsigned int* d_phase_cnt = nullptr;   // [kEngMaxPhases + 1]
-  bool engine_on = false;
-  bool lm_engine = false;                // per-launch path: LM head as a one-phase engine program
-  bool attn_coop = false;                // split-KV merge inside the attention kernel when its grid fits
   bool attn_umma = true;                 // bf16 attention on tcgen05 (else the mma.sync kernel)
   int gemm_ctas = 0;                     // stand-alone GEMM CTAs per SM the grid is sized for (0: by width)
-  // 16-KB weight boxes of the next GEMM its predecessor prefetches into L2 (0:
-  // none, the default: measured slower at every budget on the bench's drafts)
-  int l2_next = 0;
   int gemm_smem_kb = 0;                  // stand-alone GEMM stage-ring budget per CTA (0: by CTAs per SM)
   bool gemm_pairs = true;                // two token tiles of a split operand per CTA
   bool gemm_direct = true;               // single-split tiles: epilogue straight from tensor memory
@@ -370,9 +350,6 @@ struct dflash_ctx {
   float* d_ss_ctx = nullptr;             // [H / 128][128] folded-norm sums of the pending rows
   bool bn8 = true;                       // split-operand token tiles in steps of 8 rows (else 16)
   bool split_ops = true;                 // GEMM token operands as split bf16 (hi + lo) when M <= 128
-  bool cluster_red = false;              // split-K reductions through thread-block clusters (DSMEM)
-  bool lm_two_per_sm = true;             // LM-head program with two CTAs per SM
-  int engine_prefetch = 0;               // weight boxes per CTA pulled into L2 ahead of the ring
 
   // tracing (event pairs, round-robin) and launch accounting
   std::vector<cudaEvent_t> ev;
@@ -491,7 +468,6 @@ struct GemmOp {
   int rows_max = 0, t0 = 0;
   int* splits_out = nullptr;      // EPI_PARTIAL: receives the number of K splits in ws
   bool trace = true;              // false: the caller traces this launch with what follows it
-  const struct GemmNext* next = nullptr;   // the GEMM launched after this one (L2 prefetch)
   // EPI_QKV: the pending context rows u of an append ride along as token tile 1
   // (split bf16 [2][ctx_m][K], folded-norm sums ctx_ss [n_ss][ctx_m]; rows /
   // rows_max as for EPI_CTXKV): their K/V are written with the block's
@@ -499,19 +475,11 @@ struct GemmOp {
   int ctx_m = 0;
   const float* ctx_ss = nullptr;
 };
-// The GEMM that follows: its weight segments, shape and options.
-struct GemmNext {
-  const SegRef* segs;
-  int nseg, M, K;
-  const GemmOp* op;
-};
-
 // Launch shape of one tensor-core GEMM: token planes and tiles, weight tiles,
 // stage ring, K splits.
 struct GemmPlan {
   int N, nkb, XP, BN, t_tiles, tt, t_groups, n_tiles, stages, splits, kps;
   int resident;   // CTAs per SM at this shared-memory size (0: the kernel cannot run)
-  bool cluster;
   bool direct;    // one split: the epilogue reads the CTA's accumulator (no ws partials, no counters)
   bool wpair;     // EPI_SILU, direct: a CTA computes a gate tile and its up tile (n_tiles = pairs)
 };
@@ -535,7 +503,7 @@ GemmPlan plan_gemm(const dflash_ctx* c, int M, int K, const SegRef* segs, int ns
   // for both (one MMA per tile), instead of once per token tile
   // (a plain operand only for the partial store, whose epilogue has no per-token
   // scratch: TT * BN may reach 512 there)
-  g.tt = ((g.XP == 2 || op.epi == EPI_PARTIAL) && g.t_tiles >= 2 && op.epi != EPI_ARGMAX && !c->cluster_red &&
+  g.tt = ((g.XP == 2 || op.epi == EPI_PARTIAL) && g.t_tiles >= 2 && op.epi != EPI_ARGMAX &&
           c->gemm_pairs)
              ? 2
              : 1;
@@ -571,20 +539,13 @@ GemmPlan plan_gemm(const dflash_ctx* c, int M, int K, const SegRef* segs, int ns
   // split K so the grid fills the GPU in one wave (at least 2 k-blocks per split);
   // the tile's CTAs meet in the epilogue, so a split grid must fit one wave
   if (base < want && op.epi != EPI_ARGMAX) g.splits = std::max(1, std::min(want / base, std::max(1, g.nkb / 2)));
-  // fused epilogues reduce inside a thread-block cluster of the tile's splits
-  // (and its gate/up partner): at most 8 CTAs, and the partial tile plus the
-  // epilogue scratch must fit in the stage ring
-  const int P = op.epi == EPI_SILU ? 2 : 1;
-  g.cluster = c->cluster_red && op.epi != EPI_PARTIAL && op.epi != EPI_ARGMAX &&
-              (size_t)g.BN * kTileRows * 4 + (20u << 10) <= (size_t)g.stages * stage_bytes;
-  if (g.cluster) g.splits = std::min(g.splits, 8 / P);
   g.kps = (g.nkb + g.splits - 1) / g.splits;
   g.splits = (g.nkb + g.kps - 1) / g.kps;
   // a tile of one split owns its whole sum: the epilogue reads it from tensor
   // memory instead of a round trip of fp32 partials through L2 and a counter
   g.direct = false;
   g.wpair = false;
-  if (c->gemm_direct && g.splits == 1 && !g.cluster && op.epi != EPI_PARTIAL && op.ctx_x == nullptr) {
+  if (c->gemm_direct && g.splits == 1 && op.epi != EPI_PARTIAL && op.ctx_x == nullptr) {
     if (op.epi != EPI_SILU) {
       g.direct = true;
       g.resident = gemm_tc_resident_ctas(g.tt, true, gemm_tc_smem_bytes(g.BN, g.stages, g.XP, g.tt), n_cols);
@@ -614,22 +575,18 @@ GemmPlan plan_gemm(const dflash_ctx* c, int M, int K, const SegRef* segs, int ns
 
 // Tensor-core GEMM Y = X W^T over concatenated weight segments, M tokens, with
 // the epilogue of `op`.  x: bf16 [M, K] tokens for x_mode 0 (ignored otherwise).
-// With op.next, the epilogue threads pull the first weight boxes of every work
-// unit of the GEMM that follows into L2 while they wait on the split-K
-// reduction (HBM is idle then).
 int run_gemm_tc(dflash_ctx* c, const void* x, int M, int K, const SegRef* segs, int nseg, const GemmOp& op,
                 cudaStream_t s) {
   const GemmPlan pl = plan_gemm(c, M, K, segs, nseg, op);
   const int N = pl.N, nkb = pl.nkb, XP = pl.XP, BN = pl.BN, t_tiles = pl.t_groups, n_tiles = pl.n_tiles;
   const int stages = pl.stages, kps = pl.kps, splits = pl.splits;
-  const bool cluster = pl.cluster;
   if (pl.resident < 1) return fail(DFLASH_ERR_CUDA, "GEMM of %d shared-memory stages does not fit an SM", stages);
   const bool fuse = op.ctx_x != nullptr;
-  if (fuse && (op.epi != EPI_QKV || cluster || M > 128 || op.ctx_m > 128 || op.ctx_m < 1))
+  if (fuse && (op.epi != EPI_QKV || M > 128 || op.ctx_m > 128 || op.ctx_m < 1))
     return fail(DFLASH_ERR_UNSUPPORTED, "context rows ride only along a QKV GEMM of <= 128 rows");
   const int M_blk = M;
   if (fuse) M = 2 * BN;   // virtual tokens: block tile, then context tile
-  if (op.epi != EPI_ARGMAX && !cluster && !pl.direct) RET(ensure_ws(c, (size_t)splits * M * N, s));
+  if (op.epi != EPI_ARGMAX && !pl.direct) RET(ensure_ws(c, (size_t)splits * M * N, s));
   if (op.splits_out) *op.splits_out = splits;
   if (2 * (size_t)n_tiles * t_tiles >= kCounters) return fail(DFLASH_ERR_UNSUPPORTED, "too many GEMM tiles");
   TcGemmParams p;
@@ -659,30 +616,11 @@ int run_gemm_tc(dflash_ctx* c, const void* x, int M, int K, const SegRef* segs, 
       p.ss_ctx_ld = op.ctx_m;
     }
   }
-  if (op.next != nullptr && c->l2_next > 0 && !cluster && op.epi != EPI_PARTIAL && op.next->nseg <= kMaxNextSeg) {
-    const GemmNext& nx = *op.next;
-    const GemmPlan q = plan_gemm(c, nx.M, nx.K, nx.segs, nx.nseg, *nx.op);
-    int nt = 0;
-    for (int i = 0; i < nx.nseg; ++i) {
-      p.nx_tm[i] = *nx.segs[i].tm;
-      p.nx_seg_tile0[i] = nt;
-      nt += (nx.segs[i].rows + kTileRows - 1) / kTileRows;
-    }
-    p.nx_seg_tile0[nx.nseg] = nt;
-    p.nx_nseg = nx.nseg;
-    p.nx_interleave2 = nx.op->epi == EPI_SILU ? 1 : 0;
-    p.nx_units = q.n_tiles * q.splits;
-    p.nx_splits = q.splits;
-    p.nx_kps = q.kps;
-    p.nx_nkb = q.nkb;
-    p.nx_boxes = std::min(q.kps, std::max(1, c->l2_next / std::max(1, p.nx_units)));
-  }
   p.x_planes = XP;
   p.op16 = op.op16 ? 1 : 0;
   p.tt = pl.tt;
   p.direct = pl.direct ? 1 : 0;
   p.wpair = pl.wpair ? 1 : 0;
-  p.cluster_red = cluster ? 1 : 0;
   p.nseg = nseg;
   p.N = N;
   p.M = M;
@@ -966,14 +904,8 @@ int run_attention(dflash_ctx* c, const T* qb, T* ob, int l, int R, cudaStream_t 
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->d));
   p.flags = c->d_flags;
   p.o_plane = c->op16_now ? kF16Plane : (size_t)c->B * R * c->q_dim;
-  // merge the KV splits inside the attention kernel when its whole grid is
-  // resident at once (the splits of a group wait for each other)
-  const int64_t grid = (int64_t)p.n_splits * p.n_kv * p.n_qtiles * c->B;
-  p.counters = c->d_counters + kCounters / 2;
-  p.coop_merge = p.n_splits > 1 && c->attn_coop && grid <= (int64_t)attn_tc_resident_ctas(nw) * c->num_sms &&
-                 2 * (int64_t)p.n_kv * p.n_qtiles * c->B < kCounters / 2;
   CK(launch_attention_tc(p, nw, c->B, s));
-  c->launches += (p.n_splits > 1 && !p.coop_merge) ? 2 : 1;
+  c->launches += p.n_splits > 1 ? 2 : 1;
   return DFLASH_OK;
 }
 
@@ -1025,235 +957,6 @@ int draft_impl(dflash_ctx* c, const int32_t* anchor_dev, int K, float* logits_de
   return DFLASH_OK;
 }
 
-constexpr int kEngMaxPhases = 8 * DFLASH_MAX_LAYERS + 2;
-
-// Split count of a weight-streaming phase: about one unit per CTA, at least two
-// k-blocks per unit.
-int engine_splits(int n_tiles, int nkb, int grid) {
-  int splits = std::max(1, std::min(grid / std::max(1, n_tiles), std::max(1, nkb / 2)));
-  const int kps = (nkb + splits - 1) / splits;
-  return (nkb + kps - 1) / kps;
-}
-
-// Build (or find) the engine program of a K-token draft.  Phases per layer:
-// QKV, attention, O, gate/up, down (the LM head follows on its own kernels).
-// With lm_only, the program is the LM head alone (fed by the per-launch layers).
-int engine_program(dflash_ctx* c, int K, bool lm_only, cudaStream_t s, dflash_ctx::EngProgram** out) {
-  const dflash_config& g = c->cfg;
-  const int B = c->B, R = K + 1, M = B * R, H = c->H, G = c->num_sms;
-  const int BN = (M + 15) / 16 * 16;
-  const int XP = (c->split_ops && M <= 128) ? 2 : 1;   // token planes (MMA N = XP * BN <= 256)
-  const int n_kv = g.n_kv_heads, Gq = g.n_q_heads / n_kv;
-  const int arows = Gq * R, n_qtiles = (arows + 63) / 64, rows_pad = n_qtiles * 64;
-  // attention splits: about one unit per CTA over the batch's KV heads and query
-  // tiles, >= 2 tiles of 64 per split at the host's upper bound of the context
-  int max_tiles = 1;
-  for (int b = 0; b < B; ++b)
-    max_tiles = std::max(max_tiles, (int)((ctx_keys_ub(c, b) + R + 63) / 64));
-  const int groups = B * n_kv * n_qtiles;
-  const int a_splits = std::max(1, std::min({std::max(1, G / groups), std::max(1, max_tiles / 2), 16}));
-  for (dflash_ctx::EngProgram* pr : c->progs)
-    if (pr->K == K && pr->lm_only == (int)lm_only && (lm_only || pr->a_splits == a_splits) && pr->x_planes == XP) {
-      *out = pr;
-      return DFLASH_OK;
-    }
-  if (c->no_grow) return fail(DFLASH_ERR_CAPACITY, "draft program for K=%d not built before the no-alloc call", K);
-
-  // tensor maps: 0 = KV arena, then per layer wq wk wv wo wg wu wd, the LM head,
-  // then the token operands xn [M, H], attention output [M, q_dim], a [M, I]
-  std::vector<CUtensorMap> maps;
-  maps.push_back(c->tm_kv);
-  for (int l = 0; l < c->nl; ++l) {
-    const auto& lm = c->lmaps[l];
-    for (const CUtensorMap* m : {&lm.wq, &lm.wk, &lm.wv, &lm.wo, &lm.wg, &lm.wu, &lm.wd}) maps.push_back(*m);
-  }
-  const int m_lm = (int)maps.size();
-  maps.push_back(c->tm_lm);
-  const int m_xn = (int)maps.size(), m_ob = m_xn + 1, m_ab = m_xn + 2;
-  maps.resize(maps.size() + 3);
-  RET(tmap_tokens(&maps[m_xn], c->xn, (uint64_t)H, (uint64_t)M, 2, (uint32_t)BN));
-  RET(tmap_tokens(&maps[m_ob], c->ob, (uint64_t)c->q_dim, (uint64_t)M, 2, (uint32_t)BN));
-  RET(tmap_tokens(&maps[m_ab], c->ab, (uint64_t)c->I, (uint64_t)M, 2, (uint32_t)BN));
-
-  std::vector<EngPhase> ph;
-  size_t ws_floats = 0;
-  int cnt_pairs = 0, unit_run = 0;
-  auto base_args = [&](EngPhase& e, int epi, int nkb) {
-    memset(&e, 0, sizeof(e));
-    e.kind = ENG_GEMM;
-    e.epi = epi;
-    e.x_planes = XP;
-    e.M = M;
-    e.nkb = nkb;
-    e.flags = c->d_flags;
-    e.eps = g.rms_eps;
-    e.counters = c->d_counters;
-    e.argmax_keys = c->d_keys;
-    e.st = c->st;
-    e.kv = c->kv;
-    e.rope_turns = c->d_rope;
-    e.R = R;
-  };
-  auto gemm = [&](int epi, int K_in, int xmap, std::initializer_list<std::pair<int, int>> segs, bool pair_tiles) {
-    EngPhase e;
-    base_args(e, epi, K_in / kTileK);
-    int tiles = 0, cols = 0, i = 0;
-    for (const auto& sg : segs) {
-      e.wmap[i] = sg.first;
-      e.seg_rows[i] = sg.second;
-      e.seg_tile0[i] = tiles;
-      e.seg_col0[i] = cols;
-      tiles += (sg.second + kTileRows - 1) / kTileRows;
-      cols += sg.second;
-      ++i;
-    }
-    e.nseg = i;
-    e.seg_tile0[i] = tiles;
-    e.seg_col0[i] = cols;
-    e.N = cols;
-    e.n_tiles = tiles;
-    e.interleave2 = pair_tiles ? 1 : 0;
-    e.half_tiles = pair_tiles ? tiles / 2 : 1;
-    e.xmap = xmap;
-    e.splits = epi == EPI_ARGMAX ? 1 : engine_splits(tiles, e.nkb, G);
-    e.kb_per_split = (e.nkb + e.splits - 1) / e.splits;
-    e.units = tiles * e.splits;
-    if (epi != EPI_ARGMAX) {
-      ws_floats = std::max(ws_floats, (size_t)e.splits * M * cols);
-      e.cnt_off = 2 * cnt_pairs;
-      cnt_pairs += pair_tiles ? tiles / 2 : tiles;
-    }
-    return e;
-  };
-  const int n_ss = H / kTileRows;
-  for (int l = 0; l < (lm_only ? 0 : c->nl); ++l) {
-    const dflash_layer_weights& lw = c->w.layers[l];
-    const int mb = 1 + 7 * l;
-    EngPhase q = gemm(EPI_QKV, H, m_xn, {{mb, c->q_dim}, {mb + 1, c->kv_dim}, {mb + 2, c->kv_dim}}, false);
-    q.q_out = reinterpret_cast<__nv_bfloat16*>(c->qb);
-    q.layer = l;
-    if (l > 0) {
-      q.ss_in = c->d_ss;
-      q.n_ss = n_ss;
-      q.ss_ld = M;
-    }
-    ph.push_back(q);
-    EngPhase at;
-    base_args(at, 0, 0);
-    at.kind = ENG_ATTN;
-    at.layer = l;
-    at.amap = 0;
-    at.aq = reinterpret_cast<const __nv_bfloat16*>(c->qb);
-    at.ao = reinterpret_cast<__nv_bfloat16*>(c->ob);
-    at.n_q = g.n_q_heads;
-    at.n_kv = n_kv;
-    at.G = Gq;
-    at.arows = arows;
-    at.rows_pad = rows_pad;
-    at.n_qtiles = n_qtiles;
-    at.a_splits = a_splits;
-    at.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->d));
-    at.units = groups * a_splits;
-    at.cnt_off = 2 * cnt_pairs;
-    if (a_splits > 1) cnt_pairs += groups;
-    ph.push_back(at);
-    EngPhase o = gemm(EPI_RESID, c->q_dim, m_ob, {{mb + 3, H}}, false);
-    o.h = c->h;
-    o.ss_out = c->d_ss;
-    o.xn_out = reinterpret_cast<__nv_bfloat16*>(c->xn);
-    o.xn_gain = reinterpret_cast<const __nv_bfloat16*>(lw.mlp_norm);
-    ph.push_back(o);
-    EngPhase gu = gemm(EPI_SILU, H, m_xn, {{mb + 4, c->I}, {mb + 5, c->I}}, true);
-    gu.a_out = reinterpret_cast<__nv_bfloat16*>(c->ab);
-    gu.ss_in = c->d_ss;
-    gu.n_ss = n_ss;
-    gu.ss_ld = M;
-    ph.push_back(gu);
-    EngPhase dn = gemm(EPI_RESID, c->I, m_ab, {{mb + 6, H}}, false);
-    dn.h = c->h;
-    dn.ss_out = c->d_ss;
-    dn.xn_out = reinterpret_cast<__nv_bfloat16*>(c->xn);
-    dn.xn_gain = reinterpret_cast<const __nv_bfloat16*>(l + 1 < c->nl ? c->w.layers[l + 1].attn_norm : c->w.final_norm);
-    ph.push_back(dn);
-  }
-  if (lm_only) {
-    EngPhase lmh = gemm(EPI_ARGMAX, H, m_xn, {{m_lm, c->V}}, false);
-    lmh.ids = c->d_draft;
-    lmh.ss_in = c->d_ss;
-    lmh.n_ss = n_ss;
-    lmh.ss_ld = M;
-    ph.push_back(lmh);
-  }
-  if ((int)ph.size() > kEngMaxPhases) return fail(DFLASH_ERR_UNSUPPORTED, "too many engine phases");
-  if (2 * (size_t)cnt_pairs >= kCounters) return fail(DFLASH_ERR_UNSUPPORTED, "too many engine tiles");
-
-  auto* pr = new dflash_ctx::EngProgram();
-  c->progs.push_back(pr);
-  pr->K = K;
-  pr->a_splits = a_splits;
-  pr->lm_only = lm_only ? 1 : 0;
-  pr->n_phases = (int)ph.size();
-  pr->BN = BN;
-  pr->x_planes = XP;
-  pr->scratch = engine_scratch_bytes(!lm_only, BN);
-  // the LM-head program (no attention code) runs two CTAs per SM when their
-  // shared memory, registers and TMEM (>= 2 accumulators of XP * BN columns in
-  // 256 each, so the second CTA's allocation never waits) fit
-  pr->ctas_per_sm = 1;
-  if (lm_only && c->lm_two_per_sm && 2 * XP * BN <= 256) {
-    const int st2 = engine_stages_for(BN, XP, pr->scratch, 2);
-    if (st2 >= 3 && engine_resident_ctas(false, engine_smem_bytes(BN, XP, st2, pr->scratch)) >= 2) {
-      pr->ctas_per_sm = 2;
-      pr->stages = st2;
-    }
-  }
-  if (pr->ctas_per_sm == 1) pr->stages = engine_stages_for(BN, XP, pr->scratch, 1);
-  pr->nacc = std::min(4, (512 / pr->ctas_per_sm) / (XP * BN));   // accumulators of XP * BN TMEM columns
-  const size_t attn_floats = a_splits > 1 ? (size_t)B * n_kv * a_splits * rows_pad * 129 : 0;
-  if (injected_alloc_failure() || cudaMalloc(&pr->ws0, std::max<size_t>(1, ws_floats) * sizeof(float)) != cudaSuccess ||
-      cudaMalloc(&pr->ws1, std::max<size_t>(1, ws_floats) * sizeof(float)) != cudaSuccess ||
-      (attn_floats && cudaMalloc(&pr->attn, attn_floats * sizeof(float)) != cudaSuccess)) {
-    cudaGetLastError();
-    return fail(DFLASH_ERR_OOM, "draft engine workspaces");
-  }
-  for (size_t i = 0; i < ph.size(); ++i) {
-    EngPhase& e = ph[i];
-    e.dep = (int)i - 1;
-    e.unit_base = unit_run % G;
-    unit_run += e.units;
-    e.ws = (i & 1) ? pr->ws1 : pr->ws0;
-    if (e.kind == ENG_ATTN && a_splits > 1) {
-      e.part_o = pr->attn;
-      e.part_lse = pr->attn + (size_t)B * n_kv * a_splits * rows_pad * 128;
-    }
-  }
-  const size_t ph_bytes = ph.size() * sizeof(EngPhase);
-  const size_t map_off = (ph_bytes + 127) / 128 * 128;
-  const size_t bytes = map_off + maps.size() * sizeof(CUtensorMap);
-  if (cudaMallocHost(&pr->h_pinned, bytes) != cudaSuccess || cudaMalloc(&pr->d_phases, bytes) != cudaSuccess) {
-    cudaGetLastError();
-    return fail(DFLASH_ERR_OOM, "draft engine program");
-  }
-  memcpy(pr->h_pinned, ph.data(), ph_bytes);
-  memcpy(static_cast<char*>(pr->h_pinned) + map_off, maps.data(), maps.size() * sizeof(CUtensorMap));
-  pr->d_maps = reinterpret_cast<CUtensorMap*>(reinterpret_cast<char*>(pr->d_phases) + map_off);
-  CK(cudaMemcpyAsync(pr->d_phases, pr->h_pinned, bytes, cudaMemcpyHostToDevice, s));
-  *out = pr;
-  return DFLASH_OK;
-}
-
-// Algorithmic HBM bytes of one engine launch: every weight once (the draft
-// layers; or the LM head alone for the LM-head program) plus the context K/V
-// each layer reads (host upper bound of the
-// context, plus the block rows).
-double engine_bytes(const dflash_ctx* c, int K, bool lm_only) {
-  const double H = c->H, I = c->I, qd = c->q_dim, kd = c->kv_dim;
-  if (lm_only) return 2.0 * c->V * H + 2.0 * c->B * (K + 1) * H;
-  double bytes = 2.0 * c->nl * (H * (qd + 2 * kd) + qd * H + 2 * H * I + I * H);
-  for (int b = 0; b < c->B; ++b)
-    bytes += 2.0 * c->nl * 2 * kd * (double)(ctx_keys_ub(c, b) + K + 1);
-  return bytes;
-}
 
 int lm_head_bf16(dflash_ctx* c, int K, float* logits_dev, cudaStream_t s, bool op16 = false);
 
@@ -1330,51 +1033,6 @@ bool ensure_w16(dflash_ctx* c, cudaStream_t s) {
 int lm_head_rows(dflash_ctx* c, int M, cudaStream_t s);
 int flush_pending(dflash_ctx* c, cudaStream_t s);
 
-// One launch of an engine program (one CTA per SM).
-int launch_program(dflash_ctx* c, const dflash_ctx::EngProgram* pr, float* logits_dev, double bytes, cudaStream_t s) {
-  EngParams P;
-  memset(&P, 0, sizeof(P));
-  P.phases = pr->d_phases;
-  P.n_phases = pr->n_phases;
-  P.maps = pr->d_maps;
-  P.phase_cnt = c->d_phase_cnt;
-  P.flags = c->d_flags;
-  P.logits = logits_dev;
-  P.BN = pr->BN;
-  P.stages = pr->stages;
-  P.nacc = pr->nacc;
-  P.x_planes = pr->x_planes;
-  P.prefetch = c->engine_prefetch;
-  P.scratch_bytes = (uint32_t)pr->scratch;
-  const int tr = trace_begin(c, pr->lm_only ? DFLASH_TRACE_GEMM : DFLASH_TRACE_ENGINE, bytes, s);
-  CK(launch_engine(P, !pr->lm_only, pr->ctas_per_sm * c->num_sms, s));
-  trace_end(c, tr, s);
-  c->launches += 1;
-  return DFLASH_OK;
-}
-
-// Whether the draft of this K runs on the engine: bf16 with one token tile.
-bool engine_eligible(const dflash_ctx* c, int K) {
-  return c->engine_on && c->bf16 && c->d == 128 && c->B * (K + 1) <= 128 && c->nl * 5 + 1 <= kEngMaxPhases &&
-         c->cond == DFLASH_COND_KV;
-}
-
-int draft_engine(dflash_ctx* c, const int32_t* anchor_dev, int K, float* logits_dev, cudaStream_t s) {
-  const dflash_config& g = c->cfg;
-  using bf = __nv_bfloat16;
-  RET(flush_pending(c, s));
-  dflash_ctx::EngProgram* pr = nullptr;
-  RET(engine_program(c, K, false, s, &pr));
-  launch_embed_norm<bf>(reinterpret_cast<const bf*>(c->w.embed), anchor_dev, c->st, c->B, K + 1, c->H, c->V,
-                        g.mask_token_id, reinterpret_cast<const bf*>(c->w.layers[0].attn_norm), g.rms_eps, c->h,
-                        reinterpret_cast<bf*>(c->xn), (size_t)c->B * (K + 1) * c->H, c->d_flags, c->kseq_dev, s);
-  RET(launch_program(c, pr, logits_dev, engine_bytes(c, K, false), s));
-  c->launches += 1;   // the embedding
-  // the LM head streams on its own kernels: a plain weight stream with no
-  // cross-CTA dependency is fastest as a stand-alone GEMM
-  return lm_head_bf16(c, K, logits_dev, s);
-}
-
 // bf16 draft on fused tensor-core GEMMs.  Per layer: QKV (epilogue: RMSNorm
 // row scale, RoPE, q, block K/V slots) -> attention -> O (epilogue: residual,
 // sums of squares, rows * mlp_norm gain) -> gate/up (epilogue: row scale,
@@ -1389,7 +1047,7 @@ int draft_bf16(dflash_ctx* c, const int32_t* anchor_dev, int K, float* logits_de
   // above 128 rows the split operands' doubled tensor work bounds the GEMMs:
   // there every token operand is one fp16 plane (11 significant bits) against
   // the fp16 weight copies
-  const bool op16 = c->f16_ops && !c->target && M > 128 && c->d == 128 && !c->lm_engine && ensure_w16(c, s);
+  const bool op16 = c->f16_ops && !c->target && M > 128 && c->d == 128 && ensure_w16(c, s);
   c->op16_now = op16;   // read by the attention launches
   struct Op16Scope {
     dflash_ctx* c;
@@ -1409,8 +1067,7 @@ int draft_bf16(dflash_ctx* c, const int32_t* anchor_dev, int K, float* logits_de
   // one token tile each, else on their own first
   const bool fuse_ctx = c->pending && M <= 128 && c->pend_m <= 128;
   if (c->pending && !fuse_ctx) RET(flush_pending(c, s));
-  // per layer: QKV, attention, O, gate/up, down; each GEMM prefetches the first
-  // weight boxes of the GEMM after it into L2 while it reduces
+  // per layer: QKV, attention, O, gate/up, down
   struct LayerOps {
     SegRef qkv[3], wo[1], gu[2], wd[1];
     GemmOp oq, oo, og, od;
@@ -1470,24 +1127,12 @@ int draft_bf16(dflash_ctx* c, const int32_t* anchor_dev, int K, float* logits_de
     L.od = L.oo;
     L.od.xn_gain = l + 1 < c->nl ? c->w.layers[l + 1].attn_norm : c->w.final_norm;
   };
-  SegRef lmh[1] = {{op16 ? c->lm16 : c->w.lm_head, c->V, op16 ? &c->tm_lm16 : &c->tm_lm}};
-  GemmOp olm;   // the LM head's launch shape (its weights are prefetched by the last down projection)
-  olm.epi = c->lm_fused ? EPI_ARGMAX : EPI_PARTIAL;
-  olm.op16 = op16;
   LayerOps L[2];
   build(0, L[0]);
   for (int l = 0; l < c->nl; ++l) {
     LayerOps& cur = L[l & 1];
     LayerOps& nxt = L[(l + 1) & 1];
     if (l + 1 < c->nl) build(l + 1, nxt);
-    const GemmNext n_o{cur.wo, 1, M, c->q_dim, &cur.oo};
-    const GemmNext n_gu{cur.gu, 2, M, H, &cur.og};
-    const GemmNext n_d{cur.wd, 1, M, c->I, &cur.od};
-    const GemmNext n_q = l + 1 < c->nl ? GemmNext{nxt.qkv, 3, M, H, &nxt.oq} : GemmNext{lmh, 1, M, H, &olm};
-    cur.oq.next = &n_o;
-    cur.oo.next = &n_gu;
-    cur.og.next = &n_d;
-    cur.od.next = &n_q;
     RET(run_gemm_tc(c, xn, M, H, cur.qkv, 3, cur.oq, s));
     RET(run_attention<bf>(c, reinterpret_cast<const bf*>(c->qb), reinterpret_cast<bf*>(c->ob), l, R, s));
     RET(run_gemm_tc(c, c->ob, M, c->q_dim, cur.wo, 1, cur.oo, s));
@@ -1535,13 +1180,13 @@ int lm_head_bf16(dflash_ctx* c, int K, float* logits_dev, cudaStream_t s, bool o
   const void* xn = c->xn;
   // (the fused-argmax GEMM, DFLASH_LM_FUSED=1, measured at 1088 / 1025 / 257
   // rows: 1265 / 1320 / 453 us against 1299 / 1116 / 320 us for this path)
-  if (!(M <= 256 && c->lm_engine) && !c->lm_fused) {
+  if (!c->lm_fused) {
     // the LM head streams its weights in a plain partial-store GEMM (raw dot
     // products, fp32; L2-resident at drafting sizes) and a separate kernel
     // applies the final norm's row scale and takes the argmax: faster than any
-    // fused epilogue measured (125 + ~6 us vs 148 us for the persistent program
-    // at 17 rows; 963 us for the fused-argmax GEMM at 257 rows, which streams
-    // the weights once per token tile)
+    // fused epilogue measured (125 + ~6 us vs 148 us for a persistent one-phase
+    // program at 17 rows; 963 us for the fused-argmax GEMM at 257 rows, which
+    // streams the weights once per token tile)
     SegRef lmh[1] = {{op16 ? c->lm16 : c->w.lm_head, c->V, op16 ? &c->tm_lm16 : &c->tm_lm}};
     GemmOp oh;
     oh.epi = EPI_PARTIAL;
@@ -1559,14 +1204,6 @@ int lm_head_bf16(dflash_ctx* c, int K, float* logits_dev, cudaStream_t s, bool o
     CK(cudaGetLastError());
     trace_end(c, tr, s);
     c->launches += 1;
-    return DFLASH_OK;
-  }
-  if (M <= 256 && c->lm_engine) {
-    // the LM head as a one-phase persistent program: one CTA per SM streams its
-    // vocabulary tiles back to back while the argmax of the previous tile runs
-    dflash_ctx::EngProgram* pr = nullptr;
-    RET(engine_program(c, K, true, s, &pr));
-    RET(launch_program(c, pr, logits_dev, engine_bytes(c, K, true), s));
     return DFLASH_OK;
   }
   SegRef lmh[1] = {{op16 ? c->lm16 : c->w.lm_head, c->V, op16 ? &c->tm_lm16 : &c->tm_lm}};
@@ -1757,14 +1394,6 @@ void free_ctx(dflash_ctx* c) {
   if (c->ev_fork) cudaEventDestroy(c->ev_fork);
   if (c->ev_join) cudaEventDestroy(c->ev_join);
   for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
-  for (dflash_ctx::EngProgram* pr : c->progs) {
-    void* dp[] = {pr->d_phases, pr->d_maps, pr->ws0, pr->ws1, pr->attn};
-    for (void* q : dp)
-      if (q) cudaFree(q);
-    if (pr->h_pinned) cudaFreeHost(pr->h_pinned);
-    delete pr;
-  }
-  if (c->d_phase_cnt) cudaFree(c->d_phase_cnt);
   void* ptrs[] = {c->d_i32, c->d_kv_base, c->d_flags, c->d_draft, c->d_targets, c->d_rope, c->arena_raw, c->h,
                   c->xn, c->qb, c->ob, c->ab, c->xf, c->ws, c->stage, c->ub, c->attn_ws, c->d_keys,
                   c->d_counters, c->d_ss, c->ybuf, c->d_ss_ctx, c->d_ulast, c->d_seq_order, c->w16};
@@ -1932,7 +1561,6 @@ static int create_impl(const dflash_config* cfg, const dflash_weights* w, int32_
       !dalloc((void**)&c->d_keys, sizeof(unsigned long long) * kKeyStride * kKeySlots * (size_t)B * g.k_max) ||
       !dalloc((void**)&c->d_counters, sizeof(unsigned int) * kCounters) ||
       !dalloc((void**)&c->d_ss_ctx, sizeof(float) * (size_t)(c->H / kTileRows + 1) * 128) ||
-      !dalloc((void**)&c->d_phase_cnt, sizeof(unsigned int) * (kEngMaxPhases + 1)) ||
       (g.conditioning == DFLASH_COND_INPUT && !dalloc((void**)&c->d_ulast, sizeof(float) * (size_t)B * c->H)) ||
       !dalloc((void**)&c->d_seq_order, sizeof(int32_t) * (size_t)B))
     return bail(fail(DFLASH_ERR_OOM, "state allocation failed"));
@@ -1954,17 +1582,6 @@ static int create_impl(const dflash_config* cfg, const dflash_weights* w, int32_
   c->st = SeqState{c->d_ctx_len, c->d_kv_len,  c->d_anchor, c->d_cap, c->d_kv_base, c->d_pend_base,
                    c->d_rblk,    c->d_ulast, c->cond == DFLASH_COND_KV ? 1 : 0};
   {
-    // 1: the bf16 draft runs on the persistent draft engine (one launch) instead
-    // of one launch per projection / attention
-    const char* e = getenv("DFLASH_ENGINE");
-    c->engine_on = e && e[0] == '1';
-    // 1: merge the KV splits inside the attention kernel (its CTAs then hold
-    // their SMs while they wait for each other, which delays the next launch's
-    // weight prefetch; measured slower than the separate merge launch)
-    const char* am = getenv("DFLASH_ATTN_COOP");
-    c->attn_coop = am && am[0] == '1';
-    const char* ln = getenv("DFLASH_L2_NEXT");
-    if (ln) c->l2_next = std::max(0, std::min(1 << 16, atoi(ln)));
     const char* b8 = getenv("DFLASH_BN8");
     c->bn8 = !(b8 && b8[0] == '0');
     const char* fa = getenv("DFLASH_FUSE_APPEND");   // 1: defer small appends' K/V into the next draft
@@ -1985,29 +1602,15 @@ static int create_impl(const dflash_config* cfg, const dflash_weights* w, int32_
     c->gemm_smem_kb = gs ? std::max(0, std::min(200, atoi(gs))) : 0;
     const char* au = getenv("DFLASH_ATTN_UMMA");   // 0: the mma.sync attention kernel
     c->attn_umma = !(au && au[0] == '0');
-    // 1: split-K reductions of the fused epilogues inside thread-block clusters
-    // (distributed shared memory); measured slower under programmatic overlap,
-    // because a cluster starts only when one GPC has room for all its CTAs
-    const char* cr = getenv("DFLASH_CLUSTER");
-    c->cluster_red = cr && cr[0] == '1';
-    const char* l2s = getenv("DFLASH_LM_2CTA");      // 0: LM-head program with one CTA per SM
-    c->lm_two_per_sm = !(l2s && l2s[0] == '0');
     const char* sp = getenv("DFLASH_SPLIT");        // 0: plain bf16 token operands everywhere
     c->split_ops = !(sp && sp[0] == '0');
     const char* f16 = getenv("DFLASH_F16_OPS");     // 0: no fp16 operands (split bf16 above 128 rows too)
     c->f16_ops = !(f16 && f16[0] == '0');
-    // 1: the LM head (<= 256 rows) as a one-phase persistent engine program with
-    // the argmax fused, instead of a partial-store GEMM and an argmax kernel
-    const char* lmx = getenv("DFLASH_LM_ENGINE");
-    c->lm_engine = lmx && lmx[0] == '1';
-    const char* pf = getenv("DFLASH_ENGINE_PREFETCH");
-    if (pf) c->engine_prefetch = std::max(0, atoi(pf));
   }
   c->ss_rows = std::max<size_t>((size_t)c->M_max, 4096);
   if (!dalloc((void**)&c->d_ss, sizeof(float) * (size_t)std::max(1, c->H / kTileRows) * c->ss_rows))
     return bail(fail(DFLASH_ERR_OOM, "state allocation failed"));
-  if (cudaMemset(c->d_phase_cnt, 0, sizeof(unsigned int) * (kEngMaxPhases + 1)) != cudaSuccess ||
-      cudaMemset(c->d_counters, 0, sizeof(unsigned int) * kCounters) != cudaSuccess ||
+  if (cudaMemset(c->d_counters, 0, sizeof(unsigned int) * kCounters) != cudaSuccess ||
       cudaMemset(c->d_keys, 0, sizeof(unsigned long long) * kKeyStride * kKeySlots * (size_t)B * g.k_max) != cudaSuccess ||
       cudaMemset(c->d_i32, 0, sizeof(int32_t) * (size_t)B * 12) != cudaSuccess ||
       cudaMemset(c->d_kv_base, 0, 8 * (size_t)B) != cudaSuccess || cudaMemset(c->d_flags, 0, 16) != cudaSuccess)
@@ -2213,9 +1816,7 @@ int dflash_draft_block_k(dflash_ctx* c, const int32_t* anchor_ids, int32_t K, co
   auto body = [&](cudaStream_t st) -> int {
     const int tr = trace_begin(c, DFLASH_TRACE_DRAFT, 0.0, st);
     c->kseq_dev = kseq_dev;   // read by the embedding kernel, which records K_b + 1 per sequence
-    int r = !c->bf16 ? draft_impl<float>(c, anchor_dev, K, nullptr, st)
-            : engine_eligible(c, K) ? draft_engine(c, anchor_dev, K, logits_dev, st)
-                                    : draft_bf16(c, anchor_dev, K, logits_dev, st);
+    int r = !c->bf16 ? draft_impl<float>(c, anchor_dev, K, nullptr, st) : draft_bf16(c, anchor_dev, K, logits_dev, st);
     c->kseq_dev = nullptr;
     if (r != DFLASH_OK) return r;
     if (kseq_dev) {   // ids past a sequence's own K are -1

@@ -2,8 +2,8 @@
 // (128 threads, epilogue thread r = TMEM lane r = weight-tile row r) that meet
 // on named barrier 1: split-K reduction in split order, the folded RMSNorm row
 // scale, RoPE + KV-slot writes, residual + sums of squares, SwiGLU, and the
-// bounded cross-CTA counter waits.  Shared by the stand-alone GEMM kernel and
-// the draft engine.
+// bounded cross-CTA counter waits.  Shared by the tensor-core GEMM kernel's
+// instances.
 #pragma once
 
 #include "common.cuh"
@@ -119,58 +119,6 @@ struct GlobalRed {
   }
   __device__ __forceinline__ void pair(int t0, int n, float (&a0)[kRedTok], float (&a1)[kRedTok]) const {
     red_tokens2(*p, t0, n, col[0], col[1], a0, a1);
-  }
-};
-
-// barrier over every thread of every CTA of the cluster (release / acquire)
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t rank) {
-  uint32_t out;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_addr), "r"(rank));
-  return out;
-}
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-// partials in the shared memory of the cluster's CTAs: each holds its fp32 tile
-// as buf[t][128] at the same offset; split s of tile `which` is cluster rank
-// which + s * stride
-struct ClusterRed {
-  static constexpr bool kTmem = false;
-  uint32_t buf;       // shared address of the partial tile (same in every CTA)
-  int splits, stride, row;
-  int tbase;          // token of the tile's first column
-  __device__ __forceinline__ void operator()(int which, int t0, int n, float (&acc)[kRedTok]) const {
-#pragma unroll
-    for (int i = 0; i < kRedTok; ++i) acc[i] = 0.f;
-    for (int s0 = 0; s0 < splits; s0 += 4) {   // 4 splits x 8 tokens in flight
-      float v[4][kRedTok];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t base = cluster_map(buf, (uint32_t)(which + min(s0 + k, splits - 1) * stride));
-#pragma unroll
-        for (int i = 0; i < kRedTok; ++i)
-          v[k][i] = ld_cluster_f32(base + (uint32_t)(((t0 - tbase + min(i, n - 1)) * 128 + row) * 4));
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-#pragma unroll
-        for (int i = 0; i < kRedTok; ++i) acc[i] += (s0 + k < splits && i < n) ? v[k][i] : 0.f;
-    }
-  }
-  __device__ __forceinline__ void pair(int t0, int n, float (&a0)[kRedTok], float (&a1)[kRedTok]) const {
-    (*this)(0, t0, n, a0);
-    (*this)(1, t0, n, a1);
   }
 };
 
@@ -453,12 +401,6 @@ __device__ void epi_rope_kv(const EpiArgs& p, const Red& red, int r, int seg, in
     }
     epi_bar(bar);
   }
-}
-
-// token scratch of epi_rope_kv inside an epilogue chunk buffer `sm`
-__device__ __forceinline__ int* rope_tpos(float* sm) { return reinterpret_cast<int*>(sm + kEpiChunk * kEpiLd); }
-__device__ __forceinline__ long long* rope_tdst(float* sm) {
-  return reinterpret_cast<long long*>(rope_tpos(sm) + kEpiChunk);
 }
 
 // EPI_RESID (h += y) and EPI_Y_SS (v = y), then the tile's sum of squares per

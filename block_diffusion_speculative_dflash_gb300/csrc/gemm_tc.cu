@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
     // split-K reduction itself is left after the last CTA of the tile arrives.
     if (p.epi == EPI_ARGMAX) {
       row_scales(p, tid, n0, NT, row_sc);
-    } else if (p.epi != EPI_PARTIAL && !p.cluster_red) {
+    } else if (p.epi != EPI_PARTIAL) {
       const int members = (p.epi == EPI_SILU ? 2 : 1) * p.splits;
       const int member = (p.epi == EPI_SILU ? (tile & 1) * p.splits : 0) + split;
       const int t_end = min(n0 + NT, p.M);
@@ -316,7 +316,6 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
       const bool argmax = p.epi == EPI_ARGMAX;
       float* out = p.ws + (size_t)split * p.M * p.N;
       unsigned long long* wkeys = reinterpret_cast<unsigned long long*>(sA);   // [4][NT], ring idle now
-      float* cpart = reinterpret_cast<float*>(sA);                            // [NT][128], cluster mode
       for (int i = 0; i < TT; ++i) {      // token tile i: columns i * XP * BN .., tokens n0 + i * BN ..
         const uint32_t col0 = (uint32_t)(i * XP * BN);
         for (int c = 0; c < BN; c += 16) {
@@ -330,11 +329,7 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
           }
           const int tc = i * BN + c;   // token of v[0] within the CTA
           if (!argmax) {
-            if (p.cluster_red) {   // the partial tile stays on chip: cpart[t - n0][row]
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (c + j < BN) cpart[(tc + j) * kTileRows + warp * 32 + lane] = v[j];
-            } else if (rvalid) {
+            if (rvalid) {
 #pragma unroll
               for (int j = 0; j < 16; ++j) {   // columns past BN belong to the lo plane
                 const int t = n0 + tc + j;
@@ -378,28 +373,7 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
           atomicMax(p.argmax_keys + ((size_t)kidx * kKeySlots + (tile % kKeySlots)) * kKeyStride, key);
         }
       }
-      if (p.nx_units > 0 && tid >= 32) {
-        // HBM is idle while the tile's CTAs meet: the next GEMM's first weight
-        // boxes of its units cta, cta + G, ... into L2 (warps 1-3, fire and forget)
-        const int G = (int)(gridDim.x * gridDim.y * gridDim.z);
-        const int cta = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
-        const int mine = cta < p.nx_units ? (p.nx_units - cta + G - 1) / G : 0;
-        for (int i = tid - 32; i < mine * p.nx_boxes; i += 96) {
-          const int u = cta + (i / p.nx_boxes) * G, jb = i % p.nx_boxes;
-          const int ntile = u / p.nx_splits, nsplit = u - ntile * p.nx_splits;
-          int nseg = 0, nrow0;
-          if (p.nx_interleave2) {
-            nseg = ntile & 1;
-            nrow0 = (ntile >> 1) * kTileRows;
-          } else {
-            while (nseg + 1 < p.nx_nseg && ntile >= p.nx_seg_tile0[nseg + 1]) ++nseg;
-            nrow0 = (ntile - p.nx_seg_tile0[nseg]) * kTileRows;
-          }
-          const int kb = nsplit * p.nx_kps + jb;
-          if (jb < p.nx_kps && kb < p.nx_nkb) tma_prefetch_l2_box(&p.nx_tm[nseg], kb * kTileK, nrow0);
-        }
-      }
-      if (p.epi != EPI_PARTIAL && !p.cluster_red) {
+      if (p.epi != EPI_PARTIAL) {
         epi_bar();   // every epilogue thread's partial sums (or keys) are written
         float* sm = reinterpret_cast<float*>(sA);   // the stage ring is idle now
         if (argmax) {
@@ -467,41 +441,6 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
     }
   }
 
-  if (p.cluster_red) {
-    // Split-K reduction inside the cluster: every CTA of the tile (and its
-    // gate/up partner) left its fp32 partial tile in its own shared memory; after
-    // the cluster barrier each reduces a slice of the tokens straight from its
-    // peers' shared memory, in split order, and applies the epilogue.  Every
-    // thread of every CTA passes both barriers, on every path.
-    __syncwarp();
-    cluster_sync_all();
-    if (warp < 4 && ok) {
-      const int tid = threadIdx.x;
-      const bool pair = p.epi == EPI_SILU;
-      const int P = pair ? 2 : 1;
-      const int members = P * p.splits;
-      const int rank = (int)cluster_rank();
-      const int t_end = min(n0 + NT, p.M);
-      const int per = (t_end - n0 + members - 1) / members;
-      const int lo = min(t_end, n0 + rank * per), hi = min(t_end, lo + per);
-      float* sm = reinterpret_cast<float*>(smem + ((size_t)NT * kTileRows * 4 + 1023) / 1024 * 1024);
-      if (lo < hi) {
-        if (p.epi == EPI_QKV || p.epi == EPI_CTXKV || p.epi == EPI_SILU) row_scales(p, tid, lo, hi - lo, row_sc);
-        const ClusterRed red{smem_u32(smem), p.splits, P, tid, n0};
-        const int unit = pair ? tile >> 1 : tile;
-        switch (p.epi) {
-          case EPI_QKV: epi_rope_kv(p, red, tid, seg, row0, lo, hi, sm, row_sc, false, tpos, tdst, 0); break;
-          case EPI_CTXKV: epi_rope_kv(p, red, tid, seg, row0, lo, hi, sm, row_sc, true, tpos, tdst, 0); break;
-          case EPI_RESID: epi_resid(p, red, tid, tile, seg, row0, lo, hi, sm, true); break;
-          case EPI_Y_SS: epi_resid(p, red, tid, tile, seg, row0, lo, hi, sm, false); break;
-          case EPI_SILU: epi_silu(p, red, tid, unit, lo, hi, row_sc); break;
-          default: break;
-        }
-      }
-    }
-    __syncwarp();
-    cluster_sync_all();
-  }
   if (!ok) {
     *abort_flag = 1;
     set_flag(p.flags, DFLASH_FLAG_WAIT_TIMEOUT);
@@ -596,9 +535,7 @@ cudaError_t launch_gemm_tc(const TcGemmParams& p, int n_tiles, int splits, int t
   const bool direct = p.direct != 0;
   cudaError_t e = gemm_tc_allow_smem(tt, direct, smem);
   if (e != cudaSuccess) return e;
-  const dim3 cdim = p.cluster_red ? dim3(1, p.epi == EPI_SILU ? 2 : 1, splits) : dim3(1, 1, 1);
-  e = launch_k_cluster(gemm_tc_instance(tt, direct), dim3(t_tiles, n_tiles, splits), dim3(direct ? 320 : 192), smem,
-                       cdim, s, p);
+  e = launch_k(gemm_tc_instance(tt, direct), dim3(t_tiles, n_tiles, splits), dim3(direct ? 320 : 192), smem, s, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -33,34 +33,7 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// launch_k with a thread-block cluster of cdim CTAs (1 x 1 x 1: no cluster)
-template <typename... KArgs, typename... Args>
-cudaError_t launch_k_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, dim3 cdim, cudaStream_t s,
-                             Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  int n = 0;
-  attr[n].id = cudaLaunchAttributeClusterDimension;
-  attr[n].val.clusterDim.x = cdim.x;
-  attr[n].val.clusterDim.y = cdim.y;
-  attr[n].val.clusterDim.z = cdim.z;
-  ++n;
-  if (pdl_enabled()) {
-    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n].val.programmaticStreamSerializationAllowed = 1;
-    ++n;
-  }
-  cfg.attrs = attr;
-  cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-}
-
 constexpr int kMaxSeg = 32;      // weight segments one GEMM may concatenate
-constexpr int kMaxNextSeg = 3;   // weight segments of the next GEMM a GEMM prefetches into L2
 constexpr int kTileRows = 128;   // weight rows per tensor-core tile (MMA M)
 constexpr int kTileK = 64;       // K elements per pipeline stage (one 128-byte swizzle row)
 constexpr int kKeyStride = 16;   // u64 between two argmax key slots (one 128-byte line each)
@@ -122,7 +95,7 @@ enum GemmEpi : int {
 
 // What a tensor-core GEMM's epilogue needs: shape, split-K partials, and the
 // inputs and outputs of each epilogue kind (shared by the stand-alone GEMM
-// kernel and the phases of the draft engine).
+// kernel's instances).
 struct EpiArgs {
   int epi;                      // GemmEpi
   int x_planes;                 // token operand planes: 1 (plain bf16) or 2 (split hi + lo, see split_bf16)
@@ -185,67 +158,13 @@ struct TcGemmParams : EpiArgs {
   int BN;                       // token tile (MMA N = x_planes * BN, multiple of 16, <= 256)
   int tt;                       // token tiles per CTA (weights staged once, one MMA per tile)
   int stages;
-  int cluster_red;              // 1: the splits (and gate/up pair) of a tile form a cluster and
-                                //    reduce through distributed shared memory (no global partials)
   int kb_per_split;             // 64-wide k-blocks per split
   int direct;                   // 1: one split; the epilogue reads the sums from tensor memory
                                 //    (no partials in ws, no counters)
   int wpair;                    // 1 (EPI_SILU, direct, tt = 1): CTA y computes gate tile y and up
                                 //    tile y (two weight boxes per stage, two accumulators)
-  // the GEMM launched next (nx_units > 0): the first nx_boxes weight boxes of
-  // each of its work units (tile, split) are pulled into L2 by this GEMM's
-  // epilogue threads while they wait on the split-K reduction
-  CUtensorMap nx_tm[kMaxNextSeg];
-  int nx_nseg, nx_interleave2, nx_units, nx_splits, nx_kps, nx_nkb, nx_boxes;
-  int nx_seg_tile0[kMaxNextSeg + 1];
 };
 
-// ---------------------------------------------------------------- draft engine
-// One persistent launch runs a list of phases (GEMMs with their epilogues and
-// block attentions); each CTA owns a fixed round-robin share of every phase's
-// work units and announces the phase done on phase_cnt[i] once its share is
-// complete.  The weight stream of later phases runs ahead of the data.
-enum EngKind : int { ENG_GEMM = 0, ENG_ATTN = 1 };
-
-struct alignas(16) EngPhase : EpiArgs {
-  int kind;                     // EngKind
-  int dep;                      // phase whose results this phase reads (-1: the previous kernel)
-  int unit_base;                // CTA that takes unit 0 (rotates from phase to phase)
-  int units;                    // work units of the phase
-  int cnt_off;                  // first of this phase's arrival/departure counter pairs
-  // GEMM: unit u = tile * splits + split
-  int wmap[kMaxSeg];            // tensor-map index of each weight segment
-  int xmap;                     // tensor-map index of the token operand [M, K]
-  int kb_per_split, n_tiles;
-  // ATTN: unit u = ((b * n_kv + hk) * n_qtiles + qt) * a_splits + split
-  int amap;                     // tensor-map index of the KV arena
-  const __nv_bfloat16* aq;      // rotated queries [M, n_q * 128]
-  __nv_bfloat16* ao;            // attention output, split bf16 [2][M][n_q * 128]
-  float* part_o;                // [B, n_kv, a_splits, rows_pad, 128] (a_splits > 1)
-  float* part_lse;              // [B, n_kv, a_splits, rows_pad], log2 domain
-  int n_q, n_kv, G, arows, rows_pad, n_qtiles, a_splits;
-  float scale_log2;
-};
-
-struct EngParams {
-  const EngPhase* phases;       // device
-  int n_phases;
-  const CUtensorMap* maps;      // device, 64-byte aligned
-  unsigned int* phase_cnt;      // [n_phases + 1] (the last counts finished CTAs); zero between launches
-  uint32_t* flags;
-  float* logits;                // optional fp32 logits of the mask rows [B][K][V] (this call's buffer)
-  int BN, stages, nacc;
-  int x_planes;                 // token operand planes of every GEMM phase (2: split bf16)
-  int prefetch;                 // weight boxes the HBM -> L2 prefetch runs ahead of the ring (0: off)
-  uint32_t scratch_bytes;       // the K/V ring / epilogue scratch region (engine_scratch_bytes)
-};
-
-constexpr int kEngThreads = 256;
-size_t engine_smem_bytes(int BN, int x_planes, int stages, size_t scratch_bytes);
-size_t engine_scratch_bytes(bool attention, int BN);
-int engine_stages_for(int BN, int x_planes, size_t scratch_bytes, int ctas_per_sm);
-int engine_resident_ctas(bool attention, size_t smem);
-cudaError_t launch_engine(const EngParams& p, bool attention, int grid, cudaStream_t s);
 
 // Parameters of the tensor-core attention (bf16, head_dim 128).
 struct AttnTcParams {
@@ -261,11 +180,6 @@ struct AttnTcParams {
   float scale_log2;             // d^-1/2 * log2(e)
   uint32_t* flags;
   size_t o_plane;               // elements between the hi and lo planes of o (M * n_q * 128)
-  // n_splits > 1: when coop_merge, the splits of a (sequence, KV head, query
-  // tile) meet on counters[2 * group] (the whole grid must be resident) and each
-  // merges a slice of the rows; otherwise a separate merge kernel runs
-  unsigned int* counters;
-  int coop_merge;
 };
 // tcgen05 attention (head_dim 128, 128 % G == 0): query tiles of JT = 128 / G
 // block rows x G heads, loaded through tm_q = q viewed as [M][n_q][128] with
@@ -293,7 +207,6 @@ cudaError_t launch_attn_merge(const float* part_o, const float* part_lse, int n_
                               int R, int G, int n_q, __nv_bfloat16* o, size_t o_plane, int B, cudaStream_t s,
                               uint32_t* flags);
 size_t attn_tc_smem_bytes();
-int attn_tc_resident_ctas(int n_consumer_warps);   // CTAs of attn_tc_kernel resident per SM
 cudaError_t launch_attention_tc(const AttnTcParams& p, int n_consumer_warps, int B, cudaStream_t s);
 void launch_argmax_finalize(unsigned long long* keys, int rows, int32_t* ids, cudaStream_t s);
 

@@ -37,7 +37,6 @@ def _with_env(env, fn):
 @pytest.mark.parametrize("shape_kw,env", [
     (dict(), {}),
     (dict(dtype="bf16", head_dim=128), {}),
-    (dict(dtype="bf16", head_dim=128), {"DFLASH_ENGINE": "1"}),
     (dict(dtype="bf16", head_dim=128), {"DFLASH_ATTN_UMMA": "0"}),
 ])
 def test_per_sequence_k_loop_matches_oracle(shape_kw, env):

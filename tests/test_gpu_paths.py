@@ -1,8 +1,7 @@
 """GPU: the optional execution paths selected at context creation give the
 default path's results on the same state -- the mma.sync attention kernel
-instead of the tcgen05 one (DFLASH_ATTN_UMMA=0), with its split-KV merge inside
-the kernel (DFLASH_ATTN_COOP=1), the LM head as a one-phase persistent program
-with the argmax fused (DFLASH_LM_ENGINE=1) or as one GEMM with the argmax in its
+instead of the tcgen05 one (DFLASH_ATTN_UMMA=0, the kernel of head counts whose
+group size does not divide 128), the LM head as one GEMM with the argmax in its
 epilogue (DFLASH_LM_FUSED=1) -- and the default path (partial-store LM-head
 GEMM + argmax kernel) stays within the oracle's bf16 tolerance; loops with the
 appends' K/V projected inside the next draft's QKV GEMMs (DFLASH_FUSE_APPEND=1)
@@ -44,8 +43,7 @@ def _run(s, Wd, ctx, env):
     return d.cpu().numpy(), z.cpu().numpy(), st, f, anchors
 
 
-@pytest.mark.parametrize("env", [{"DFLASH_ATTN_UMMA": "0", "DFLASH_ATTN_COOP": "1"}, {"DFLASH_LM_ENGINE": "1"}, {"DFLASH_ATTN_UMMA": "0"},
-                                 {"DFLASH_LM_FUSED": "1"}])
+@pytest.mark.parametrize("env", [{"DFLASH_ATTN_UMMA": "0"}, {"DFLASH_LM_FUSED": "1"}])
 def test_optional_path_matches_default(env):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
