@@ -566,8 +566,8 @@ def main():
     traffic = lm_traffic(s, K)
     da_gbs = draft_bytes / (ms_da / 1e3) / 1e9
     it_gbs = (draft_bytes + append_bytes) / (ms_it / 1e3) / 1e9
-    lm_kernel = ("gemm_tc_kernel (tcgen05 weight stream, fp32 partial store) + lm_argmax_kernel"
-                 if s.dtype == "bf16" else "gemm_simt_kernel + argmax_kernel")
+    lm_kernel = ("gemm_tc_kernel (LM head: tcgen05 weight stream, fp32 partial store; the argmax kernel after it "
+                 "is not in this figure)" if s.dtype == "bf16" else "gemm_simt_kernel (LM head)")
 
     out = {
         "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world, "steps": args.steps,

@@ -1193,16 +1193,12 @@ int lm_head_bf16(dflash_ctx* c, int K, float* logits_dev, cudaStream_t s, bool o
     oh.op16 = op16;
     int splits = 1;
     oh.splits_out = &splits;
-    oh.trace = false;
-    // traced as one LM-head operation: weights + tokens in, ids (+ logits) out
-    const double lm_bytes = 2.0 * ((double)c->V * H + (double)M * H) + 4.0 * B * K * (logits_dev ? c->V + 1.0 : 1.0);
-    const int tr = trace_begin(c, DFLASH_TRACE_GEMM, lm_bytes, s);
+    // traced as a GEMM of its own (weights and tokens in, fp32 dot products out)
     RET(run_gemm_tc(c, xn, M, H, lmh, 1, oh, s));
     // its arrival counter is the last one, which no GEMM or attention tile uses
     launch_lm_argmax(c->ws, splits, M, c->V, R, c->d_ss, n_ss, M, H, g.rms_eps, logits_dev, c->d_keys,
                      c->d_counters + kCounters - 1, c->d_draft, B * K, s);
     CK(cudaGetLastError());
-    trace_end(c, tr, s);
     c->launches += 1;
     return DFLASH_OK;
   }
