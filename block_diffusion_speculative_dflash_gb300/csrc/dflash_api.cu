@@ -321,6 +321,10 @@ struct dflash_ctx {
   // allocation, made at the first draft of more than 128 rows): the tensor
   // cores take fp16 token operands only against fp16 weights
   bool f16_ops = true;                       // DFLASH_F16_OPS=0: split bf16 operands at every M
+  // fp16 operands from this many GEMM rows up (DFLASH_F16_MIN_ROWS): from 33 the
+  // split operand's second MMA and wider token boxes cost more than fp16's
+  // coarser rounding is worth (Llama-3.1-8B shape, batch 8: 1264 -> 1077 us)
+  int f16_min_rows = 33;
   bool op16_now = false;                     // the running draft's token operands are fp16
   bool w16_failed = false;
   char* w16 = nullptr;
@@ -1044,10 +1048,10 @@ int draft_bf16(dflash_ctx* c, const int32_t* anchor_dev, int K, float* logits_de
   const dflash_config& g = c->cfg;
   using bf = __nv_bfloat16;
   bf* xn = reinterpret_cast<bf*>(c->xn);
-  // above 128 rows the split operands' doubled tensor work bounds the GEMMs:
-  // there every token operand is one fp16 plane (11 significant bits) against
-  // the fp16 weight copies
-  const bool op16 = c->f16_ops && !c->target && M > 128 && c->d == 128 && ensure_w16(c, s);
+  // from f16_min_rows GEMM rows the split operands' doubled tensor work and
+  // token boxes cost more than they buy: there every token operand is one fp16
+  // plane (11 significant bits) against the fp16 weight copies
+  const bool op16 = c->f16_ops && !c->target && M >= c->f16_min_rows && c->d == 128 && ensure_w16(c, s);
   c->op16_now = op16;   // read by the attention launches
   struct Op16Scope {
     dflash_ctx* c;
@@ -1065,7 +1069,7 @@ int draft_bf16(dflash_ctx* c, const int32_t* anchor_dev, int K, float* logits_de
   const int n_ss = H / kTileRows;
   // a pending append's K/V are projected with the layers' QKV when both fit
   // one token tile each, else on their own first
-  const bool fuse_ctx = c->pending && M <= 128 && c->pend_m <= 128;
+  const bool fuse_ctx = c->pending && M <= 128 && c->pend_m <= 128 && !op16;   // (its rows are split bf16)
   if (c->pending && !fuse_ctx) RET(flush_pending(c, s));
   // per layer: QKV, attention, O, gate/up, down
   struct LayerOps {
@@ -1600,8 +1604,10 @@ static int create_impl(const dflash_config* cfg, const dflash_weights* w, int32_
     c->attn_umma = !(au && au[0] == '0');
     const char* sp = getenv("DFLASH_SPLIT");        // 0: plain bf16 token operands everywhere
     c->split_ops = !(sp && sp[0] == '0');
-    const char* f16 = getenv("DFLASH_F16_OPS");     // 0: no fp16 operands (split bf16 above 128 rows too)
+    const char* f16 = getenv("DFLASH_F16_OPS");     // 0: no fp16 operands (split bf16 at every M)
     c->f16_ops = !(f16 && f16[0] == '0');
+    const char* fm = getenv("DFLASH_F16_MIN_ROWS");
+    if (fm) c->f16_min_rows = std::max(1, atoi(fm));
   }
   c->ss_rows = std::max<size_t>((size_t)c->M_max, 4096);
   if (!dalloc((void**)&c->d_ss, sizeof(float) * (size_t)std::max(1, c->H / kTileRows) * c->ss_rows))

@@ -77,7 +77,7 @@ typedef enum { DFLASH_COND_KV = 0, DFLASH_COND_INPUT = 1, DFLASH_COND_NONE = 2 }
 #define DFLASH_FLAG_WAIT_TIMEOUT   0x8u  /* a bounded mbarrier wait ran out: kernel returned */
 #define DFLASH_FLAG_BAD_ROWS       0x10u /* append row count outside [0, rows_max]: clamped */
 #define DFLASH_FLAG_BAD_K          0x20u /* per-sequence K outside [1, K]: clamped */
-#define DFLASH_FLAG_F16_RANGE      0x40u /* an fp16 GEMM operand (drafts of > 128 rows) outside
+#define DFLASH_FLAG_F16_RANGE      0x40u /* an fp16 GEMM operand (drafts of >= 33 rows) outside
                                             +-65504 or NaN: the value was stored as fp16 inf/NaN */
 
 /* Drafter shape.  All matrix widths must be multiples of 64; head_dim 64 or 128;
@@ -187,8 +187,10 @@ int dflash_ctx_append(dflash_ctx* ctx, const void* feats, int32_t rows_max,
  * while the arguments and the context's workspaces stay the same; inside a
  * caller's stream capture, with host anchors or with tracing on it launches
  * eagerly (environment DFLASH_GRAPH=0: always).
- * A bf16 draft of more than 128 rows (B * (K + 1)) with head_dim 128 feeds the
- * tensor cores fp16 token operands against fp16 copies of the layer and
+ * A bf16 draft of 33 rows or more (B * (K + 1); environment DFLASH_F16_MIN_ROWS
+ * moves the threshold) with head_dim 128 feeds the tensor cores fp16 token
+ * operands (11 significant bits) instead of split bf16 ones (about 16), against
+ * fp16 copies of the layer and
  * LM-head weights, which the first such draft makes (one allocation of the
  * weights' size, kept until dflash_destroy; the weights must not change
  * afterwards); without the memory, inside a stream capture, in

@@ -46,7 +46,7 @@ def test_llama31_8b_batch8_sampled():
     for it in range(3):
         rep = sb.step(it, 2e-2)
         compared += rep["ids_compared"]
-        print(f"llama31_8b batch 8 (split operands) it {it}: max rel logit err {rep['max_rel']:.4f}")
+        print(f"llama31_8b batch 8 (fp16 operands, 88 rows) it {it}: max rel logit err {rep['max_rel']:.4f}")
     assert compared >= 6
     del sb
     torch.cuda.empty_cache()
@@ -108,9 +108,9 @@ def test_serving_batch64_32_iterations_sampled():
 
 def test_llama31_8b_batch12_f16_operands_sampled():
     """The Llama-3.1-8B shape (the tightest logit-error budget of the workloads)
-    with batch 12: 132 GEMM rows, so every projection takes fp16 token operands
-    against the fp16 weight copies; the shortest-context sequence against the
-    oracle over 2 iterations, same criteria."""
+    with batch 12: 132 GEMM rows of fp16 token operands against the fp16 weight
+    copies (more than one 128-row token tile); the shortest-context sequence
+    against the oracle over 2 iterations, same criteria."""
     torch = _cuda()
     s = CONFIGS["llama31_8b"].with_(batch=12)
     assert s.batch * (s.K + 1) > 128

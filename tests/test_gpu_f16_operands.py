@@ -1,9 +1,9 @@
-"""GPU: fp16 token operands.  Above 128 GEMM rows a bf16 draft stores every
+"""GPU: fp16 token operands.  From 33 GEMM rows a bf16 draft stores every
 projection's token operand as one fp16 plane and multiplies it with fp16
 copies of the weights, instead of split bf16 (two planes, twice the tensor
 work).  The drafts must still meet the logit tolerance against the oracle;
-the mode must engage above 128 rows (the logits differ from the split ones)
-and nowhere else (bit-identical at 128 rows or fewer)."""
+the mode must engage from 33 rows (the logits differ from the split ones)
+and nowhere else (bit-identical at 32 rows or fewer)."""
 import numpy as np
 import pytest
 
@@ -51,8 +51,8 @@ def _draft(torch, s, W_dev, ctx):
     return out
 
 
-@pytest.mark.parametrize("batch,K,engaged", [(12, 15, True), (8, 15, False)])
-def test_f16_operands_engage_above_128_rows_only(monkeypatch, batch, K, engaged):
+@pytest.mark.parametrize("batch,K,engaged", [(12, 15, True), (3, 10, True), (2, 15, False), (1, 16, False)])
+def test_f16_operands_engage_from_33_rows_only(monkeypatch, batch, K, engaged):
     torch = _cuda()
     s = _shape(batch, K)
     W_dev = upload_weights(make_weights(s))
@@ -61,7 +61,7 @@ def test_f16_operands_engage_above_128_rows_only(monkeypatch, batch, K, engaged)
     monkeypatch.setenv("DFLASH_F16_OPS", "0")
     z_split = _draft(torch, s, W_dev, ctx)
     if engaged:
-        assert not np.array_equal(z_default, z_split), "fp16 operands did not engage at 192 rows"
+        assert not np.array_equal(z_default, z_split), f"fp16 operands did not engage at {batch * (K + 1)} rows"
         assert row_rel_err(z_default.reshape(-1, s.vocab), z_split.reshape(-1, s.vocab)).max() <= 2e-2
     else:
-        assert np.array_equal(z_default, z_split), "the operand format changed at 128 rows"
+        assert np.array_equal(z_default, z_split), f"the operand format changed at {batch * (K + 1)} rows"
