@@ -8,15 +8,18 @@
 // One CTA = (KV split, KV head x query tile, sequence).  A query tile is 128
 // rows: JT = 128 / G consecutive block rows j times the G query heads of the KV
 // head, row r = jj * G + g, loaded by one 3-D TMA box per half of head_dim.
-//   warp 4   producer: the query tile once, then 64-position K and V tiles of
+//   warp 8   producer: the query tile once, then 64-position K and V tiles of
 //            the KV arena into a 3-stage ring (two 64 x 64 boxes per operand,
 //            128-byte swizzle)
-//   warp 5   TMEM owner and MMA issuer: S = Q K^T (M = 128 rows, N = 64
+//   warp 9   TMEM owner and MMA issuer: S = Q K^T (M = 128 rows, N = 64
 //            positions, K = 128) into one of two TMEM score buffers, then
 //            O += P V (N = 128 dims, K = 64 positions; V is read as an MN-major
 //            operand straight from the TMA layout) into the TMEM output
-//   warps 0-3 softmax, one query row per thread (TMEM lane = row): scores to
-//            registers, log2-domain softmax against a reference maximum that is
+//   warps 0-7 softmax, two threads per query row (TMEM lane = row; warps w and
+//            w + 4 share the lane quarter w, each takes one half of a tile's 64
+//            positions and of the 128 output dimensions): scores to registers,
+//            the row maximum of the tile from both halves (exchanged in shared
+//            memory), log2-domain softmax against a reference maximum that is
 //            only raised when a row's maximum grows by more than kRescale (then
 //            the row of O is rescaled in TMEM), P as split bf16 (hi + lo planes,
 //            two MMAs, ~16 significant bits) into shared memory, and at the end
@@ -98,6 +101,31 @@ __device__ __forceinline__ void st_swizzled_row(uint8_t* tile, int r, const uint
     *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 }
 
+// Half a row: chunks c0 .. c0 + 3 (32 bf16) of row r of such a tile.
+__device__ __forceinline__ void st_swizzled_half(uint8_t* tile, int r, int c0, const uint32_t (&w)[16]) {
+  uint8_t* row = tile + (size_t)r * 128;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(row + (((c0 + c) ^ (r & 7)) << 4)) =
+        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+
+// The two softmax warps of TMEM lane quarter q (w and w + 4) meet on named
+// barrier 1 + q; the _and form also returns whether v held in all 64 threads,
+// so that both warps leave the tile loop on the same tile and meet the same
+// number of times on every path.
+__device__ __forceinline__ void quarter_bar(int q) { asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory"); }
+__device__ __forceinline__ bool quarter_bar_and(int q, bool v) {
+  uint32_t all;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, 64, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(all)
+      : "r"((uint32_t)v), "r"(1 + q)
+      : "memory");
+  return all != 0;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -117,7 +145,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return okv != 0;
 }
 
-__global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant__ AttnUParams p) {
+constexpr int kUThreads = 320;   // 8 softmax warps, the producer, the MMA issuer
+
+__global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_constant__ AttnUParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -137,6 +167,9 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
   uint64_t* mma_done = o_final + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // the two halves' tile maxima [tile parity][half][row] and row sums [half][row]
+  float* xmax = reinterpret_cast<float*>(tmem_slot + 4);
+  float* xsum = xmax + 2 * 2 * 128;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -147,8 +180,8 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&s_free[i], 8);
+      mbar_init(&p_full[i], 8);
       mbar_init(&p_free[i], 1);
     }
     mbar_init(o_done, 1);
@@ -157,7 +190,7 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, kUTmemCols);
     tmem_relinquish();
   }
@@ -192,7 +225,7 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
   bool ok = true;
   int issued = 0;
   bool q_issued = false;
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------ producer
     if (lane == 0 && ntiles > 0) {
       tma_prefetch_desc(&p.tm_q);
@@ -218,7 +251,7 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
         issued = t + 1;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0 && ntiles > 0) {
       const uint32_t idesc_s = umma_idesc_bf16(128, kUTile);
@@ -269,41 +302,53 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
     }
     if (lane == 0) umma_commit(mma_done);   // tracks every MMA issued above
   } else {
-    // ------------------------------------------------ softmax, one query row per thread
-    const int r = threadIdx.x;                          // 0..127 = TMEM lane = tile row
+    // ------------------------------------------------ softmax, two threads per query row
+    const int r = threadIdx.x & 127;                    // TMEM lane = tile row
+    const int hf = threadIdx.x >> 7;                    // half: positions 32 hf .. of a tile, dims 64 hf ..
+    const int qq = warp & 3;                            // TMEM lane quarter
     const int gq = r % p.G, j = qt * p.JT + r / p.G;    // query head hk * G + gq, block row j
     const bool rvalid = j < p.R;
     const int row_lim = block_base(p.st, b) + j;   // causal: the row's own position
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float m_ref = -INFINITY, l = 0.f;
+    const uint32_t lane_base = (uint32_t)(qq * 32) << 16;
+    float m_ref = -INFINITY, l = 0.f;   // l: this half's share of the row sum
+    // a failed wait skips the rest of its tile; the pair leaves the loop
+    // together at the next meeting
     for (int t = 0; t < ntiles; ++t) {
       const int sb = t & 1;
-      if (!warp_wait(&s_full[sb], (uint32_t)((t >> 1) & 1), abort_flag, p.flags)) {
+      float s[kUTile / 2];
+      float hmax = -INFINITY;
+      if (ok && warp_wait(&s_full[sb], (uint32_t)((t >> 1) & 1), abort_flag, p.flags)) {
+        tc_fence_after();
+        tmem_ld32_issue(tmem + lane_base + (uint32_t)(sb * kUTile + 32 * hf), s);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[sb]);
+        // scale into the log2 domain; positions past the split (and, causal,
+        // past the row's own position) are masked
+        const int pos0 = p_begin + t * kUTile + 32 * hf;
+        const int p_row = p.causal ? min(p_end, row_lim + 1) : p_end;
+#pragma unroll
+        for (int i = 0; i < kUTile / 2; ++i) {
+          const float v = pos0 + i < p_row ? s[i] * p.scale_log2 : -INFINITY;
+          s[i] = v;
+          hmax = fmaxf(hmax, v);
+        }
+      } else {
+        ok = false;
+      }
+      // the row's maximum over the whole tile: this half's and the partner's
+      // (double-buffered by tile parity, so one meeting per tile suffices)
+      xmax[(sb * 2 + hf) * 128 + r] = hmax;
+      if (!quarter_bar_and(qq, ok)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      float s[kUTile];
-#pragma unroll
-      for (int c = 0; c < kUTile; c += 32) tmem_ld32_issue(tmem + lane_base + (uint32_t)(sb * kUTile + c), s + c);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
-      // scale into the log2 domain; positions past the split (and, causal,
-      // past the row's own position) are masked
-      const int pos0 = p_begin + t * kUTile;
-      const int p_row = p.causal ? min(p_end, row_lim + 1) : p_end;
-      float tmax = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kUTile; ++i) {
-        const float v = pos0 + i < p_row ? s[i] * p.scale_log2 : -INFINITY;
-        s[i] = v;
-        tmax = fmaxf(tmax, v);
-      }
+      const float tmax = fmaxf(hmax, xmax[(sb * 2 + (hf ^ 1)) * 128 + r]);
       // reference maximum: set by the first tile (which always holds the
       // split's first position), raised only when a row outgrows it by more
-      // than kRescale -- then O and l of that row are rescaled
+      // than kRescale -- then O and l of that row are rescaled (both halves
+      // take the same decision from the same maximum)
       float factor = 1.f;
       bool resc = false;
       if (t == 0) {
@@ -313,16 +358,16 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
         m_ref = tmax;
         resc = true;
       }
-      if (__any_sync(0xffffffffu, resc)) {   // the warp rescales its 32 rows of O (PV of tile t-1 done)
+      if (__any_sync(0xffffffffu, resc)) {   // the warp rescales its half of its 32 rows of O (PV of tile t-1 done)
         // S(t) was committed after PV(t-2) and PV(t) waits for this tile's P, so
         // o_done is in phase t-1 or t: the parity wait is unambiguous
         if (!warp_wait(o_done, (uint32_t)((t - 1) & 1), abort_flag, p.flags)) {
           ok = false;
-          break;
+          continue;
         }
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 16) {
+        for (int c = 64 * hf; c < 64 * hf + 64; c += 16) {
           float o16[16];
           tmem_ld16(tmem + lane_base + 128u + (uint32_t)c, o16);
 #pragma unroll
@@ -336,10 +381,10 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
       // (a causal row may see no position of this split: its scores are all
       // -inf, and so is m_ref; 0 as the reference makes P = 0, l = 0)
       const float mr = m_ref == -INFINITY ? 0.f : m_ref;
-      uint32_t hi[kUTile / 2], lo[kUTile / 2];
+      uint32_t hi[kUTile / 4], lo[kUTile / 4];
       float ps = 0.f;
 #pragma unroll
-      for (int i = 0; i < kUTile / 2; ++i) {
+      for (int i = 0; i < kUTile / 4; ++i) {
         const float p0 = exp2f(s[2 * i] - mr), p1 = exp2f(s[2 * i + 1] - mr);
         ps += p0 + p1;
         const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
@@ -350,20 +395,25 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
       const int pb = t & 1;
       if (!warp_wait(&p_free[pb], (uint32_t)((t >> 1) & 1) ^ 1u, abort_flag, p.flags)) {
         ok = false;
-        break;
+        continue;
       }
-      st_swizzled_row(sP + (size_t)(pb * 2) * kUPPlane, r, hi);
-      st_swizzled_row(sP + (size_t)(pb * 2 + 1) * kUPPlane, r, lo);
+      st_swizzled_half(sP + (size_t)(pb * 2) * kUPPlane, r, 4 * hf, hi);
+      st_swizzled_half(sP + (size_t)(pb * 2 + 1) * kUPPlane, r, 4 * hf, lo);
       fence_proxy_async_smem();   // generic-proxy P writes -> the tensor core's reads
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[pb]);
     }
     // ------------------------------------------------ output: O / l
+    // the row sum from both halves, in half order (both threads get the same
+    // value); every softmax thread meets its partner here on every path
+    xsum[hf * 128 + r] = l;
+    quarter_bar(qq);
+    const float lrow = xsum[r] + xsum[128 + r];
     if (ok) {
       const int qd = p.n_q * 128;
-      const float inv = l > 0.f ? 1.0f / l : 0.f;
-      const float lse = l > 0.f ? m_ref + log2f(l) : -INFINITY;
+      const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
+      const float lse = lrow > 0.f ? m_ref + log2f(lrow) : -INFINITY;
       // the last PV has its own barrier: by now o_done may be anywhere between
       // the last two phases, so a parity wait on it would be ambiguous
       const bool have = ntiles > 0 && warp_wait(o_final, 0u, abort_flag, p.flags);
@@ -373,8 +423,8 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
         const int rq = gq * p.R + j;   // row of the merge kernel's layout
         const size_t prow = (((size_t)(b * p.n_kv + hk) * p.n_splits + split) * p.rows_pad + rq);
         __nv_bfloat16* orow = p.o + (size_t)(b * p.R + j) * qd + (size_t)(hk * p.G + gq) * 128;
-#pragma unroll 1
-        for (int h = 0; h < 128; h += 64) {   // 64 output columns per batch of TMEM loads
+        {
+          const int h = 64 * hf;   // this half's 64 output columns in one batch of TMEM loads
           float o64[64];
           if (have) {
             tmem_ld32_issue(tmem + lane_base + 128u + (uint32_t)h, o64);
@@ -384,48 +434,50 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
 #pragma unroll
             for (int i = 0; i < 64; ++i) o64[i] = 0.f;
           }
-          if (!rvalid) continue;
+          if (rvalid) {
 #pragma unroll
-          for (int cc = 0; cc < 64; cc += 16) {
-            const float* o16 = o64 + cc;
-            const int c = h + cc;
-            if (p.n_splits == 1 && p.o_plane == kF16Plane) {   // one fp16 plane
-              uint32_t wh[8];
+            for (int cc = 0; cc < 64; cc += 16) {
+              const float* o16 = o64 + cc;
+              const int c = h + cc;
+              if (p.n_splits == 1 && p.o_plane == kF16Plane) {   // one fp16 plane
+                uint32_t wh[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                check_f16(o16[2 * i] * inv, p.flags);
-                check_f16(o16[2 * i + 1] * inv, p.flags);
-                const __half2 v = __floats2half2_rn(o16[2 * i] * inv, o16[2 * i + 1] * inv);
-                wh[i] = *reinterpret_cast<const uint32_t*>(&v);
+                for (int i = 0; i < 8; ++i) {
+                  check_f16(o16[2 * i] * inv, p.flags);
+                  check_f16(o16[2 * i + 1] * inv, p.flags);
+                  const __half2 v = __floats2half2_rn(o16[2 * i] * inv, o16[2 * i + 1] * inv);
+                  wh[i] = *reinterpret_cast<const uint32_t*>(&v);
+                }
+                uint4* dh = reinterpret_cast<uint4*>(orow + c);
+                dh[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                dh[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
+              } else if (p.n_splits == 1) {   // split bf16: hi plane, lo plane o_plane further
+                uint32_t wh[8], wl[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  __nv_bfloat16 h0, l0, h1, l1;
+                  split_bf16(o16[2 * i] * inv, &h0, &l0);
+                  split_bf16(o16[2 * i + 1] * inv, &h1, &l1);
+                  wh[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                  wl[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                }
+                uint4* dh = reinterpret_cast<uint4*>(orow + c);
+                uint4* dl = reinterpret_cast<uint4*>(orow + p.o_plane + c);
+                dh[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                dh[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
+                dl[0] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+                dl[1] = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+              } else {
+                float4* po = reinterpret_cast<float4*>(p.part_o + prow * 128 + c);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  po[i] = make_float4(o16[4 * i] * inv, o16[4 * i + 1] * inv, o16[4 * i + 2] * inv,
+                                      o16[4 * i + 3] * inv);
               }
-              uint4* dh = reinterpret_cast<uint4*>(orow + c);
-              dh[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-              dh[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
-            } else if (p.n_splits == 1) {   // split bf16: hi plane, lo plane o_plane further
-              uint32_t wh[8], wl[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                __nv_bfloat16 h0, l0, h1, l1;
-                split_bf16(o16[2 * i] * inv, &h0, &l0);
-                split_bf16(o16[2 * i + 1] * inv, &h1, &l1);
-                wh[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-                wl[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-              }
-              uint4* dh = reinterpret_cast<uint4*>(orow + c);
-              uint4* dl = reinterpret_cast<uint4*>(orow + p.o_plane + c);
-              dh[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-              dh[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
-              dl[0] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-              dl[1] = make_uint4(wl[4], wl[5], wl[6], wl[7]);
-            } else {
-              float4* po = reinterpret_cast<float4*>(p.part_o + prow * 128 + c);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                po[i] = make_float4(o16[4 * i] * inv, o16[4 * i + 1] * inv, o16[4 * i + 2] * inv, o16[4 * i + 3] * inv);
             }
           }
         }
-        if (rvalid && p.n_splits > 1) p.part_lse[prow] = lse;
+        if (rvalid && p.n_splits > 1 && hf == 0) p.part_lse[prow] = lse;
       }
     }
   }
@@ -436,13 +488,13 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
   }
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag && warp == 4 && lane == 0) {
+  if (*abort_flag && warp == 8 && lane == 0) {
     // let every load still in flight land before the shared memory goes away
     if (q_issued) (void)mbar_wait(q_full, 0u, nullptr);
     for (int t = max(0, issued - kUStages); t < issued; ++t)
       (void)mbar_wait(&kv_full[t % kUStages], (uint32_t)((t / kUStages) & 1), nullptr);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     if (lane == 0) (void)mbar_wait(mma_done, 0u, nullptr);   // MMAs done before TMEM is freed
     __syncwarp();
     tc_fence_after();
@@ -453,7 +505,8 @@ __global__ void __launch_bounds__(192, 1) attn_umma_kernel(const __grid_constant
 }  // namespace
 
 size_t attn_umma_smem_bytes() {
-  return 1024 + 2 * kUQHalf + kUStages * kUStage + 4 * kUPPlane + (1 + 2 * kUStages + 8 + 3) * 8 + 16;
+  return 1024 + 2 * kUQHalf + kUStages * kUStage + 4 * kUPPlane + (1 + 2 * kUStages + 8 + 3) * 8 + 16 +
+         (2 * 2 * 128 + 2 * 128) * sizeof(float);
 }
 
 cudaError_t launch_attention_umma(const AttnUParams& p, int B, cudaStream_t s) {
@@ -464,7 +517,7 @@ cudaError_t launch_attention_umma(const AttnUParams& p, int B, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  launch_k(attn_umma_kernel, dim3(p.n_splits, p.n_kv * p.n_qtiles, B), dim3(192), smem, s, p);
+  launch_k(attn_umma_kernel, dim3(p.n_splits, p.n_kv * p.n_qtiles, B), dim3(kUThreads), smem, s, p);
   return cudaGetLastError();
 }
 
