@@ -268,14 +268,21 @@ __global__ void __launch_bounds__(128) attn_merge_dim_kernel(const float* __rest
                                                              const float* __restrict__ part_lse, int n_kv, int S,
                                                              int rows, int rows_pad, int R, int G, int n_q,
                                                              __nv_bfloat16* __restrict__ o, size_t o_plane,
-                                                             uint32_t* flags) {
+                                                             uint32_t* flags, const int32_t* __restrict__ seq_split) {
   pdl_trigger();
   pdl_wait();
   __shared__ float w_s[kMergeBatch];
   __shared__ float mx_s;
   const int r = blockIdx.x, hk = blockIdx.y, b = blockIdx.z, d = threadIdx.x;
   if (r >= rows) return;
-  const size_t base = (size_t)(b * n_kv + hk) * S * rows_pad + r;
+  size_t base;
+  if (seq_split != nullptr) {   // per-sequence splits; one split was written directly
+    S = seq_split[2 * b];
+    if (S <= 1) return;
+    base = ((size_t)seq_split[2 * b + 1] * n_kv + (size_t)hk * S) * rows_pad + r;
+  } else {
+    base = (size_t)(b * n_kv + hk) * S * rows_pad + r;
+  }
   float v[kMergeBatch];
 #pragma unroll
   for (int k = 0; k < kMergeBatch; ++k) v[k] = k < S ? __ldcg(part_o + (base + (size_t)k * rows_pad) * 128 + d) : 0.f;
@@ -332,13 +339,21 @@ __global__ void __launch_bounds__(32 * kMergeRows) attn_merge_kernel(const float
                                                                     const float* __restrict__ part_lse, int n_kv,
                                                                     int S, int rows, int rows_pad, int R, int G,
                                                                     int n_q, __nv_bfloat16* __restrict__ o,
-                                                                    size_t o_plane, uint32_t* flags) {
+                                                                    size_t o_plane, uint32_t* flags,
+                                                                    const int32_t* __restrict__ seq_split) {
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), hk = blockIdx.y, b = blockIdx.z;
   if (r >= rows) return;   // (whole warps)
-  const size_t base = (size_t)(b * n_kv + hk) * S * rows_pad + r;
+  size_t base;
+  if (seq_split != nullptr) {   // per-sequence splits; one split was written directly
+    S = seq_split[2 * b];
+    if (S <= 1) return;
+    base = ((size_t)seq_split[2 * b + 1] * n_kv + (size_t)hk * S) * rows_pad + r;
+  } else {
+    base = (size_t)(b * n_kv + hk) * S * rows_pad + r;
+  }
   float mx = -INFINITY;
   for (int s0 = 0; s0 < S; s0 += 32)
     mx = fmaxf(mx, s0 + lane < S ? __ldcg(part_lse + base + (size_t)(s0 + lane) * rows_pad) : -INFINITY);
@@ -398,7 +413,7 @@ size_t attn_tc_smem_bytes() { return 1024 + kStages * kStageBytes + 2 * kStages 
 
 cudaError_t launch_attn_merge(const float* part_o, const float* part_lse, int n_kv, int S, int rows, int rows_pad,
                               int R, int G, int n_q, __nv_bfloat16* o, size_t o_plane, int B, cudaStream_t s,
-                              uint32_t* flags) {
+                              uint32_t* flags, const int32_t* seq_split) {
   // rows per CTA: up to kMergeRows while the grid still gives every SM about two CTAs
   static int n_sm = 0;
   if (n_sm == 0) {
@@ -414,20 +429,20 @@ cudaError_t launch_attn_merge(const float* part_o, const float* part_lse, int n_
   }
   if (mode == 1 || (mode == 0 && total < 8 * 2 * (int64_t)n_sm)) {
     launch_k(attn_merge_dim_kernel, dim3(rows, n_kv, B), dim3(128), 0, s, part_o, part_lse, n_kv, S, rows, rows_pad, R,
-             G, n_q, o, o_plane, flags);
+             G, n_q, o, o_plane, flags, seq_split);
     return cudaGetLastError();
   }
   const int rpc = (int)std::max<int64_t>(1, std::min<int64_t>(kMergeRows, total / (2 * (int64_t)n_sm)));
   const dim3 grid((rows + rpc - 1) / rpc, n_kv, B), block(32 * rpc);
   if (S <= 4)
     launch_k(attn_merge_kernel<4>, grid, block, 0, s, part_o, part_lse, n_kv, S, rows, rows_pad, R, G, n_q, o, o_plane,
-             flags);
+             flags, seq_split);
   else if (S <= 16)
     launch_k(attn_merge_kernel<16>, grid, block, 0, s, part_o, part_lse, n_kv, S, rows, rows_pad, R, G, n_q, o, o_plane,
-             flags);
+             flags, seq_split);
   else
     launch_k(attn_merge_kernel<32>, grid, block, 0, s, part_o, part_lse, n_kv, S, rows, rows_pad, R, G, n_q, o, o_plane,
-             flags);
+             flags, seq_split);
   return cudaGetLastError();
 }
 

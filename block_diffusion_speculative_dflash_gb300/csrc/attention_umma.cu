@@ -5,16 +5,26 @@
 // applies -- every query row of a KV head (G query heads x R block rows)
 // attends to all kv_len_b context slots and all R block slots of its sequence.
 //
-// One CTA = (KV split, KV head x query tile, sequence).  A query tile is 128
-// rows: JT = 128 / G consecutive block rows j times the G query heads of the KV
-// head, row r = jj * G + g, loaded by one 3-D TMA box per half of head_dim.
-//   warp 8   producer: the query tile once, then 64-position K and V tiles of
-//            the KV arena into a 3-stage ring (two 64 x 64 boxes per operand,
-//            128-byte swizzle)
+// A work item = (sequence, KV head x query tile, KV split).  A query tile is
+// 128 rows: JT = 128 / G consecutive block rows j times the G query heads of
+// the KV head, row r = jj * G + g, loaded by one 3-D TMA box per half of
+// head_dim.  A batch's items come from a schedule planned on the device once
+// per draft (splits per sequence from its live length, longest items first)
+// and are taken by one persistent CTA per SM; a single sequence runs one item
+// per CTA from the grid.  Roles:
+//   warp 8   item fetch (persistent: from the launch's counter, published to
+//            the other roles through a shared-memory slot ring), the query
+//            tile of each item, and the K tiles (64 positions, two 64 x 64
+//            boxes, 128-byte swizzle) into a 3-stage ring
+//   warp 10  the V tiles into the same stages; K and V of a stage have
+//            barriers of their own, so the next K may land as soon as S has
+//            read the last one while PV still reads V
 //   warp 9   TMEM owner and MMA issuer: S = Q K^T (M = 128 rows, N = 64
 //            positions, K = 128) into one of two TMEM score buffers, then
 //            O += P V (N = 128 dims, K = 64 positions; V is read as an MN-major
-//            operand straight from the TMA layout) into the TMEM output
+//            operand straight from the TMA layout) into one of two TMEM output
+//            buffers (alternating by item, so that one item's output phase
+//            overlaps the next item's MMAs)
 //   warps 0-7 softmax, two threads per query row (TMEM lane = row; warps w and
 //            w + 4 share the lane quarter w, each takes one half of a tile's 64
 //            positions and of the 128 output dimensions): scores to registers,
@@ -41,7 +51,7 @@ constexpr uint32_t kUStage = 4 * kUBox;               // K[0:64], K[64:128], V[0
 constexpr uint32_t kUQHalf = 128 * 128;               // [128 rows][64 dims] bf16
 constexpr uint32_t kUPPlane = 128 * 128;              // [128 rows][64 positions] bf16
 constexpr float kRescale = 8.0f;                      // log2 headroom of P before O is rescaled
-constexpr uint32_t kUTmemCols = 256;                  // S[2] (2 x 64) + O (128)
+constexpr uint32_t kUTmemCols = 512;                  // S[2] (2 x 64) + O[2] (2 x 128); grid mode: one O
 
 // 32 lanes x 32 bits, 16 consecutive columns written from the thread's row.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
@@ -92,16 +102,9 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16_bmn(int M, int N) {
   return umma_idesc_bf16(M, N) | (1u << 16);
 }
 
-// One row (64 bf16 = 8 chunks of 16 B) of a K-major, 128-byte-swizzled tile
-// whose base is 1024-B aligned: chunk c of row r sits at chunk c ^ (r & 7).
-__device__ __forceinline__ void st_swizzled_row(uint8_t* tile, int r, const uint32_t (&w)[32]) {
-  uint8_t* row = tile + (size_t)r * 128;
-#pragma unroll
-  for (int c = 0; c < 8; ++c)
-    *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-}
-
-// Half a row: chunks c0 .. c0 + 3 (32 bf16) of row r of such a tile.
+// Half a row (chunks c0 .. c0 + 3, 32 bf16) of row r of a K-major,
+// 128-byte-swizzled tile whose base is 1024-B aligned: chunk c of row r sits
+// at chunk c ^ (r & 7).
 __device__ __forceinline__ void st_swizzled_half(uint8_t* tile, int r, int c0, const uint32_t (&w)[16]) {
   uint8_t* row = tile + (size_t)r * 128;
 #pragma unroll
@@ -145,8 +148,72 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return okv != 0;
 }
 
-constexpr int kUThreads = 320;   // 8 softmax warps, the producer, the MMA issuer
+constexpr int kUThreads = 352;   // 8 softmax warps, the query/K producer, the MMA issuer, the V producer
+constexpr int kUSlots = 4;       // work items published ahead of the consumers
+constexpr int kUItem = 10;       // ints per published item
 
+// One work item: query tile qt of KV head hk of sequence b against the
+// sequence's KV split `split` of S, positions [p_begin, p_end); partials of a
+// sequence with S > 1 go to partial group pg + split (b < 0: no more items);
+// rowK / rowV: the arena rows of the head's K and V at position 0.
+struct UItem {
+  int b, split, hk, qt, p_begin, p_end, S, pg, rowK, rowV;
+};
+
+// Item w of the launch: from the grid (one item per CTA), or the w-th of the
+// persistent schedule (units in the planned order, every head-tile of a unit
+// consecutive); the split's range is the balanced share of the live length.
+template <bool grid_mode>
+__device__ __forceinline__ UItem decode_item(const AttnUParams& p, int w) {
+  UItem x;
+  const int n_hq = p.n_kv * p.n_qtiles;
+  int hq;
+  if constexpr (grid_mode) {
+    x.b = p.seq_order != nullptr ? p.seq_order[blockIdx.z] : blockIdx.z;
+    x.split = blockIdx.x;
+    hq = blockIdx.y;
+    x.S = p.n_splits;
+    x.pg = x.b * x.S;
+  } else {
+    const int unit = p.work[w / n_hq];
+    hq = w % n_hq;
+    x.b = unit >> 8;
+    x.split = unit & 255;
+    x.S = p.seq_split[2 * x.b];
+    x.pg = p.seq_split[2 * x.b + 1];
+  }
+  x.hk = hq % p.n_kv;
+  x.qt = hq / p.n_kv;
+  // every load of the sequence's state at once (one round trip)
+  const int cap = p.st.cap[x.b];
+  const int64_t kv_base = p.st.kv_base[x.b];
+  int L = block_base(p.st, x.b) + p.st.rblk[x.b];   // context + this sequence's K_b + 1 block rows
+  x.rowK = (int)kv_row(p.kv, kv_base, cap, p.layer, 0, x.hk, 0);
+  x.rowV = (int)kv_row(p.kv, kv_base, cap, p.layer, 1, x.hk, 0);
+  if (L > cap) {
+    if (x.split == 0 && hq == 0) set_flag(p.flags, DFLASH_FLAG_CAPACITY);
+    L = cap;
+  }
+  // balanced split of [0, L) into S ranges of whole tiles (live length)
+  const int chunk = ((L + x.S - 1) / x.S + kUTile - 1) / kUTile * kUTile;
+  x.p_begin = x.split * chunk;
+  x.p_end = min(L, x.p_begin + chunk);
+  return x;
+}
+__device__ __forceinline__ int item_tiles(const UItem& x) {
+  return x.p_end > x.p_begin ? (x.p_end - x.p_begin + kUTile - 1) / kUTile : 0;
+}
+
+// Persistent (p.work set): one CTA per SM takes items from the launch's
+// counter until they run out, the producer running ahead into the next item's
+// queries and K/V while the last tiles and the output of the current one are
+// processed; two output accumulators in tensor memory let one item's output
+// phase overlap the next item's MMAs.  Grid mode (p.work null): the grid
+// (split, head x query tile, sequence) with one item per CTA.
+// (Two instances, so that the one-item-per-CTA grid carries none of the
+// persistent schedule's code: its CTAs start cold, and every instruction
+// fetched on the way to the first loads is on the critical path.)
+template <bool PERSIST>
 __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_constant__ AttnUParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -156,42 +223,61 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
   uint8_t* sP = ring + kUStages * kUStage;              // [2 buffers][hi, lo][128 rows][64 positions]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 4 * kUPPlane);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = bars + 1 + kUStages;
-  uint64_t* s_full = bars + 1 + 2 * kUStages;
+  uint64_t* q_free = bars + 1;       // the item's last S MMA is done: the next queries may land
+  // K and V of a stage have barriers of their own: a K slot is free once S has
+  // read it, a V slot once PV has
+  uint64_t* k_full = bars + 2;
+  uint64_t* k_empty = k_full + kUStages;
+  uint64_t* v_full = k_empty + kUStages;
+  uint64_t* v_empty = v_full + kUStages;
+  uint64_t* s_full = v_empty + kUStages;
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;
   uint64_t* p_free = p_full + 2;
   uint64_t* o_done = p_free + 2;     // one phase per PV (the softmax rescales after PV t-1)
-  uint64_t* o_final = o_done + 1;    // the last PV
-  uint64_t* mma_done = o_final + 1;
+  uint64_t* o_final = o_done + 1;    // [2] the last PV of an item, by output buffer
+  uint64_t* o_free = o_final + 2;    // [2] the softmax has read an output buffer
+  uint64_t* it_full = o_free + 2;    // [kUSlots] an item is published
+  uint64_t* it_free = it_full + kUSlots;   // [kUSlots] every consumer has read it
+  uint64_t* mma_done = it_free + kUSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  // the two halves' tile maxima [tile parity][half][row] and row sums [half][row]
-  float* xmax = reinterpret_cast<float*>(tmem_slot + 4);
+  int* items = reinterpret_cast<int*>(tmem_slot + 4);           // [kUSlots][kUItem]
+  // the two halves' tile maxima [tile parity][half][row] and row sums [item parity][half][row]
+  float* xmax = reinterpret_cast<float*>(items + kUSlots * kUItem);
   float* xsum = xmax + 2 * 2 * 128;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_free, 1);
     for (int i = 0; i < kUStages; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 8);
       mbar_init(&p_full[i], 8);
       mbar_init(&p_free[i], 1);
+      mbar_init(&o_final[i], 1);
+      mbar_init(&o_free[i], 8);
+    }
+    for (int i = 0; i < kUSlots; ++i) {
+      mbar_init(&it_full[i], 1);
+      mbar_init(&it_free[i], 10);   // eight softmax warps, the MMA issuer and the V producer
     }
     mbar_init(o_done, 1);
-    mbar_init(o_final, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
+  constexpr bool grid_mode = !PERSIST;
+  const uint32_t tmem_cols = grid_mode ? kUTmemCols / 2 : kUTmemCols;
   if (warp == 9) {
-    tmem_alloc(tmem_slot, kUTmemCols);
+    tmem_alloc(tmem_slot, tmem_cols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -202,103 +288,213 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
   // successor CTA that took this SM's columns first would wait for this grid
   // while this CTA waited in its allocation
   pdl_trigger();
-  pdl_wait();   // the queries and the KV arena come from the predecessors
+  pdl_wait();   // the queries, the KV arena and the schedule come from the predecessors
 
-  const int split = blockIdx.x;
-  const int hk = blockIdx.y % p.n_kv, qt = blockIdx.y / p.n_kv;
-  const int b = p.seq_order != nullptr ? p.seq_order[blockIdx.z] : blockIdx.z;
-  const int cap = p.st.cap[b];
-  int L = block_base(p.st, b) + p.st.rblk[b];   // context + this sequence's K_b + 1 block rows
-  if (L > cap) {
-    if (threadIdx.x == 0 && split == 0 && hk == 0 && qt == 0) set_flag(p.flags, DFLASH_FLAG_CAPACITY);
-    L = cap;
-  }
-  // balanced split of [0, L) into n_splits ranges of whole tiles (live length)
-  const int chunk = ((L + p.n_splits - 1) / p.n_splits + kUTile - 1) / kUTile * kUTile;
-  const int p_begin = split * chunk;
-  const int p_end = min(L, p_begin + chunk);
-  const int ntiles = p_end > p_begin ? (p_end - p_begin + kUTile - 1) / kUTile : 0;
-  const int64_t base = p.st.kv_base[b];
-  const int rowK = (int)kv_row(p.kv, base, cap, p.layer, 0, hk, 0);
-  const int rowV = (int)kv_row(p.kv, base, cap, p.layer, 1, hk, 0);
-
+  // grid mode: the CTA's one item, decoded by every thread at once
+  UItem gx;
+  if constexpr (grid_mode) gx = decode_item<true>(p, 0);
   bool ok = true;
-  int issued = 0;
-  bool q_issued = false;
+  int issued = 0, q_loads = 0;   // producers: K (or V) tiles and query tiles whose loads were issued
   if (warp == 8) {
-    // ------------------------------------------------ producer
-    if (lane == 0 && ntiles > 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_kv);
-      mbar_arrive_expect_tx(q_full, 2 * kUQHalf);
-      const int tok = b * p.R + qt * p.JT;
-      tma_load_3d(sQ, &p.tm_q, 0, hk * p.G, tok, q_full);
-      tma_load_3d(sQ + kUQHalf, &p.tm_q, 64, hk * p.G, tok, q_full);
-      q_issued = true;
-      for (int t = 0; t < ntiles; ++t) {
-        const int st = t % kUStages;
-        if (!mbar_wait(&kv_empty[st], (uint32_t)((t / kUStages) & 1) ^ 1u, abort_flag, p.flags)) {
+    // ------------------------------------------------ queries and K
+    if (lane == 0) {
+      const int n_items = grid_mode ? 1 : *p.n_units * p.n_kv * p.n_qtiles;
+      (void)n_items;
+      for (int i = 0;; ++i) {
+        UItem x;
+        if constexpr (grid_mode) {   // the CTA's one item, known to every role
+          if (i > 0) break;
+          x = gx;
+        } else {
+          const int slot = i % kUSlots;
+          if (!mbar_wait(&it_free[slot], (uint32_t)((i / kUSlots) & 1) ^ 1u, abort_flag, p.flags)) {
+            ok = false;
+            break;
+          }
+          const int w = (int)atomicAdd(p.item_ctr, 1u);
+          if (w < n_items) {
+            x = decode_item<false>(p, w);
+          } else {
+            x.b = -1;
+            x.split = x.hk = x.qt = x.p_begin = x.p_end = x.S = x.pg = x.rowK = x.rowV = 0;
+          }
+          int* it = items + slot * kUItem;
+          it[0] = x.b;
+          it[1] = x.split;
+          it[2] = x.hk;
+          it[3] = x.qt;
+          it[4] = x.p_begin;
+          it[5] = x.p_end;
+          it[6] = x.S;
+          it[7] = x.pg;
+          it[8] = x.rowK;
+          it[9] = x.rowV;
+          mbar_arrive(&it_full[slot]);   // (release: the fields above before the arrival)
+          if (x.b < 0) break;
+        }
+        const int nt = item_tiles(x);
+        if (nt == 0) continue;
+        const int rowK = x.rowK;
+        if (q_loads == 0) {   // (after the item's loads: a descriptor prefetch ahead of them delays them)
+          tma_prefetch_desc(&p.tm_q);
+          tma_prefetch_desc(&p.tm_kv);
+        }
+        // the queries: once the previous item's last S has read its own
+        if (!mbar_wait(q_free, (uint32_t)(q_loads & 1) ^ 1u, abort_flag, p.flags)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&kv_full[st], kUStage);
-        const int pos = p_begin + t * kUTile;
-        uint8_t* dst = ring + (size_t)st * kUStage;
-        tma_load_2d(dst, &p.tm_kv, 0, rowK + pos, &kv_full[st]);
-        tma_load_2d(dst + kUBox, &p.tm_kv, 64, rowK + pos, &kv_full[st]);
-        tma_load_2d(dst + 2 * kUBox, &p.tm_kv, 0, rowV + pos, &kv_full[st]);
-        tma_load_2d(dst + 3 * kUBox, &p.tm_kv, 64, rowV + pos, &kv_full[st]);
-        issued = t + 1;
+        mbar_arrive_expect_tx(q_full, 2 * kUQHalf);
+        const int tok = x.b * p.R + x.qt * p.JT;
+        tma_load_3d(sQ, &p.tm_q, 0, x.hk * p.G, tok, q_full);
+        tma_load_3d(sQ + kUQHalf, &p.tm_q, 64, x.hk * p.G, tok, q_full);
+        ++q_loads;
+        for (int t = 0; t < nt; ++t) {
+          const int g = issued, st = g % kUStages;
+          if (!mbar_wait(&k_empty[st], (uint32_t)((g / kUStages) & 1) ^ 1u, abort_flag, p.flags)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&k_full[st], 2 * kUBox);
+          const int pos = x.p_begin + t * kUTile;
+          uint8_t* dst = ring + (size_t)st * kUStage;
+          tma_load_2d(dst, &p.tm_kv, 0, rowK + pos, &k_full[st]);
+          tma_load_2d(dst + kUBox, &p.tm_kv, 64, rowK + pos, &k_full[st]);
+          issued = g + 1;
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------ V
+    if (lane == 0) {
+      for (int i = 0;; ++i) {
+        int b, p_begin, p_end, rowV;
+        if constexpr (grid_mode) {
+          if (i > 0) break;
+          b = gx.b, p_begin = gx.p_begin, p_end = gx.p_end, rowV = gx.rowV;
+        } else {
+          const int slot = i % kUSlots;
+          if (!mbar_wait(&it_full[slot], (uint32_t)((i / kUSlots) & 1), abort_flag, p.flags)) {
+            ok = false;
+            break;
+          }
+          const int* it = items + slot * kUItem;
+          b = it[0], p_begin = it[4], p_end = it[5], rowV = it[9];
+          mbar_arrive(&it_free[slot]);
+          if (b < 0) break;
+        }
+        const int nt = p_end > p_begin ? (p_end - p_begin + kUTile - 1) / kUTile : 0;
+        if (nt == 0) continue;
+        for (int t = 0; t < nt; ++t) {
+          const int g = issued, st = g % kUStages;
+          if (!mbar_wait(&v_empty[st], (uint32_t)((g / kUStages) & 1) ^ 1u, abort_flag, p.flags)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&v_full[st], 2 * kUBox);
+          const int pos = p_begin + t * kUTile;
+          uint8_t* dst = ring + (size_t)st * kUStage + 2 * kUBox;
+          tma_load_2d(dst, &p.tm_kv, 0, rowV + pos, &v_full[st]);
+          tma_load_2d(dst + kUBox, &p.tm_kv, 64, rowV + pos, &v_full[st]);
+          issued = g + 1;
+        }
+        if (!ok) break;
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------ MMA issuer
-    if (lane == 0 && ntiles > 0) {
+    if (lane == 0) {
       const uint32_t idesc_s = umma_idesc_bf16(128, kUTile);
       const uint32_t idesc_o = umma_idesc_bf16_bmn(128, 128);
       const uint64_t qa[2] = {sw128_kmajor_desc(smem_u32(sQ)), sw128_kmajor_desc(smem_u32(sQ + kUQHalf))};
-      // O += P(u) V(u): P hi and lo planes (K-major, 64 positions), V MN-major
-      // (rows = positions, 128 B of dims; the two 64-dim halves 8 KB apart)
-      auto pv = [&](int u) -> bool {
-        const int pb = u & 1, st = u % kUStages;
-        if (!mbar_wait(&p_full[pb], (uint32_t)((u >> 1) & 1), abort_flag, p.flags)) return false;
+      struct Pv {
+        int g, st, ob, mi;
+        bool first, last;
+      };
+      // O[ob] += P(g) V(g): P hi and lo planes (K-major, 64 positions), V
+      // MN-major (rows = positions, 128 B of dims; the two 64-dim halves 8 KB
+      // apart); the first PV of an item overwrites the buffer, once the softmax
+      // has read the item that used it before
+      auto pv = [&](const Pv& x) -> bool {
+        const int pb = x.g & 1;
+        if (!mbar_wait(&p_full[pb], (uint32_t)((x.g >> 1) & 1), abort_flag, p.flags) ||
+            !mbar_wait(&v_full[x.st], (uint32_t)((x.g / kUStages) & 1), abort_flag, p.flags))
+          return false;
+        if (x.first && !mbar_wait(&o_free[x.ob], (uint32_t)((x.mi >> 1) & 1) ^ 1u, abort_flag, p.flags))
+          return false;
         tc_fence_after();
-        const uint32_t vb = smem_u32(ring + (size_t)st * kUStage + 2 * kUBox);
+        const uint32_t vb = smem_u32(ring + (size_t)x.st * kUStage + 2 * kUBox);
+        const uint32_t od = tmem + 128u + 128u * (uint32_t)x.ob;
 #pragma unroll
         for (int pl = 0; pl < 2; ++pl) {
           const uint64_t pa = sw128_kmajor_desc(smem_u32(sP + (size_t)(pb * 2 + pl) * kUPPlane));
 #pragma unroll
           for (int k = 0; k < kUTile / 16; ++k)   // 16 positions = two 8-row groups = 2048 B of V
-            umma_bf16(tmem + 128u, pa + 2u * k, sw128_mnmajor_desc(vb + 2048u * k, kUBox, 1024u), idesc_o,
-                      (u | pl | k) != 0 ? 1u : 0u);
+            umma_bf16(od, pa + 2u * k, sw128_mnmajor_desc(vb + 2048u * k, kUBox, 1024u), idesc_o,
+                      (!x.first || pl != 0 || k != 0) ? 1u : 0u);
         }
-        umma_commit(&kv_empty[st]);
+        umma_commit(&v_empty[x.st]);
         umma_commit(&p_free[pb]);
         umma_commit(o_done);
+        if (x.last) umma_commit(&o_final[x.ob]);
         return true;
       };
-      if (!mbar_wait(q_full, 0u, abort_flag, p.flags)) ok = false;
-      for (int t = 0; t < ntiles && ok; ++t) {
-        const int st = t % kUStages, sb = t & 1;
-        if (!mbar_wait(&kv_full[st], (uint32_t)((t / kUStages) & 1), abort_flag, p.flags) ||
-            !mbar_wait(&s_free[sb], (uint32_t)((t >> 1) & 1) ^ 1u, abort_flag, p.flags)) {
+      int g = 0, mi = 0;   // K/V tiles and items with tiles so far
+      for (int i = 0; ok; ++i) {
+        int p_begin, p_end;
+        if constexpr (grid_mode) {
+          if (i > 0) break;
+          p_begin = gx.p_begin, p_end = gx.p_end;
+        } else {
+          const int slot = i % kUSlots;
+          if (!mbar_wait(&it_full[slot], (uint32_t)((i / kUSlots) & 1), abort_flag, p.flags)) {
+            ok = false;
+            break;
+          }
+          const int* it = items + slot * kUItem;
+          const int b = it[0];
+          p_begin = it[4], p_end = it[5];
+          mbar_arrive(&it_free[slot]);
+          if (b < 0) break;
+        }
+        const int nt = p_end > p_begin ? (p_end - p_begin + kUTile - 1) / kUTile : 0;
+        if (nt == 0) continue;
+        if (!mbar_wait(q_full, (uint32_t)(mi & 1), abort_flag, p.flags)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint8_t* kt = ring + (size_t)st * kUStage;
+        Pv prev{};
+        for (int t = 0; t < nt; ++t, ++g) {
+          const int st = g % kUStages, sb = g & 1;
+          if (!mbar_wait(&k_full[st], (uint32_t)((g / kUStages) & 1), abort_flag, p.flags) ||
+              !mbar_wait(&s_free[sb], (uint32_t)((g >> 1) & 1) ^ 1u, abort_flag, p.flags)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* kt = ring + (size_t)st * kUStage;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint64_t kd = sw128_kmajor_desc(smem_u32(kt + h * kUBox));
+          for (int h = 0; h < 2; ++h) {
+            const uint64_t kd = sw128_kmajor_desc(smem_u32(kt + h * kUBox));
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_bf16(tmem + (uint32_t)(sb * kUTile), qa[h] + 2u * k, kd + 2u * k, idesc_s, (h | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)
+              umma_bf16(tmem + (uint32_t)(sb * kUTile), qa[h] + 2u * k, kd + 2u * k, idesc_s, (h | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[sb]);
+          umma_commit(&k_empty[st]);              // K is read: the slot may take a later tile's K
+          if (t == nt - 1) umma_commit(q_free);   // the queries are read: the next item's may land
+          if (t > 0 && !pv(prev)) {
+            ok = false;
+            break;
+          }
+          prev = Pv{g, st, mi & 1, mi, t == 0, t == nt - 1};
         }
-        umma_commit(&s_full[sb]);
-        if (t > 0 && !pv(t - 1)) ok = false;
+        // the item's last PV at once, so that its output does not wait for
+        // the next item's first tile
+        if (ok && !pv(prev)) ok = false;
+        ++mi;
       }
-      if (ok && !pv(ntiles - 1)) ok = false;
-      if (ok) umma_commit(o_final);
     }
     if (lane == 0) umma_commit(mma_done);   // tracks every MMA issued above
   } else {
@@ -306,160 +502,192 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
     const int r = threadIdx.x & 127;                    // TMEM lane = tile row
     const int hf = threadIdx.x >> 7;                    // half: positions 32 hf .. of a tile, dims 64 hf ..
     const int qq = warp & 3;                            // TMEM lane quarter
-    const int gq = r % p.G, j = qt * p.JT + r / p.G;    // query head hk * G + gq, block row j
-    const bool rvalid = j < p.R;
-    const int row_lim = block_base(p.st, b) + j;   // causal: the row's own position
     const uint32_t lane_base = (uint32_t)(qq * 32) << 16;
-    float m_ref = -INFINITY, l = 0.f;   // l: this half's share of the row sum
-    // a failed wait skips the rest of its tile; the pair leaves the loop
-    // together at the next meeting
-    for (int t = 0; t < ntiles; ++t) {
-      const int sb = t & 1;
-      float s[kUTile / 2];
-      float hmax = -INFINITY;
-      if (ok && warp_wait(&s_full[sb], (uint32_t)((t >> 1) & 1), abort_flag, p.flags)) {
-        tc_fence_after();
-        tmem_ld32_issue(tmem + lane_base + (uint32_t)(sb * kUTile + 32 * hf), s);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[sb]);
-        // scale into the log2 domain; positions past the split (and, causal,
-        // past the row's own position) are masked
-        const int pos0 = p_begin + t * kUTile + 32 * hf;
-        const int p_row = p.causal ? min(p_end, row_lim + 1) : p_end;
-#pragma unroll
-        for (int i = 0; i < kUTile / 2; ++i) {
-          const float v = pos0 + i < p_row ? s[i] * p.scale_log2 : -INFINITY;
-          s[i] = v;
-          hmax = fmaxf(hmax, v);
-        }
+    int g = 0, mi = 0;   // K/V tiles and items with tiles so far
+    for (int i = 0;; ++i) {
+      UItem x;
+      if constexpr (grid_mode) {
+        if (i > 0) break;
+        x = gx;
       } else {
-        ok = false;
+        const int slot = i % kUSlots;
+        // the pair takes every item together (and leaves together on a failure)
+        const bool got = ok && warp_wait(&it_full[slot], (uint32_t)((i / kUSlots) & 1), abort_flag, p.flags);
+        if (!quarter_bar_and(qq, got)) {
+          ok = false;
+          break;
+        }
+        const int* it = items + slot * kUItem;
+        x.b = it[0], x.split = it[1], x.hk = it[2], x.qt = it[3], x.p_begin = it[4], x.p_end = it[5], x.S = it[6],
+        x.pg = it[7], x.rowK = x.rowV = 0;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&it_free[slot]);
+        if (x.b < 0) break;
       }
-      // the row's maximum over the whole tile: this half's and the partner's
-      // (double-buffered by tile parity, so one meeting per tile suffices)
-      xmax[(sb * 2 + hf) * 128 + r] = hmax;
-      if (!quarter_bar_and(qq, ok)) {
-        ok = false;
-        break;
-      }
-      const float tmax = fmaxf(hmax, xmax[(sb * 2 + (hf ^ 1)) * 128 + r]);
-      // reference maximum: set by the first tile (which always holds the
-      // split's first position), raised only when a row outgrows it by more
-      // than kRescale -- then O and l of that row are rescaled (both halves
-      // take the same decision from the same maximum)
-      float factor = 1.f;
-      bool resc = false;
-      if (t == 0) {
-        m_ref = tmax;
-      } else if (tmax > m_ref + kRescale) {
-        factor = exp2f(m_ref - tmax);
-        m_ref = tmax;
-        resc = true;
-      }
-      if (__any_sync(0xffffffffu, resc)) {   // the warp rescales its half of its 32 rows of O (PV of tile t-1 done)
-        // S(t) was committed after PV(t-2) and PV(t) waits for this tile's P, so
-        // o_done is in phase t-1 or t: the parity wait is unambiguous
-        if (!warp_wait(o_done, (uint32_t)((t - 1) & 1), abort_flag, p.flags)) {
+      const int b = x.b, split = x.split, hk = x.hk, qt = x.qt, p_begin = x.p_begin, p_end = x.p_end, S = x.S,
+                pg = x.pg;
+      const int nt = p_end > p_begin ? (p_end - p_begin + kUTile - 1) / kUTile : 0;
+      const int ob = mi & 1;
+      const int gq = r % p.G, j = qt * p.JT + r / p.G;   // query head hk * G + gq, block row j
+      const bool rvalid = j < p.R;
+      const int row_lim = block_base(p.st, b) + j;       // causal: the row's own position
+      const uint32_t o_tm = tmem + lane_base + 128u + 128u * (uint32_t)ob;
+      float m_ref = -INFINITY, l = 0.f;                  // l: this half's share of the row sum
+      // a failed wait skips the rest of its tile; the pair leaves the loop
+      // together at the next meeting
+      for (int t = 0; t < nt; ++t, ++g) {
+        const int sb = g & 1;
+        float s[kUTile / 2];
+        float hmax = -INFINITY;
+        if (ok && warp_wait(&s_full[sb], (uint32_t)((g >> 1) & 1), abort_flag, p.flags)) {
+          tc_fence_after();
+          tmem_ld32_issue(tmem + lane_base + (uint32_t)(sb * kUTile + 32 * hf), s);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[sb]);
+          // scale into the log2 domain; positions past the split (and, causal,
+          // past the row's own position) are masked
+          const int pos0 = p_begin + t * kUTile + 32 * hf;
+          const int p_row = p.causal ? min(p_end, row_lim + 1) : p_end;
+#pragma unroll
+          for (int i2 = 0; i2 < kUTile / 2; ++i2) {
+            const float v = pos0 + i2 < p_row ? s[i2] * p.scale_log2 : -INFINITY;
+            s[i2] = v;
+            hmax = fmaxf(hmax, v);
+          }
+        } else {
+          ok = false;
+        }
+        // the row's maximum over the whole tile: this half's and the partner's
+        // (double-buffered by tile parity, so one meeting per tile suffices)
+        xmax[(sb * 2 + hf) * 128 + r] = hmax;
+        if (!quarter_bar_and(qq, ok)) {
+          ok = false;
+          break;
+        }
+        const float tmax = fmaxf(hmax, xmax[(sb * 2 + (hf ^ 1)) * 128 + r]);
+        // reference maximum: set by the first tile (which always holds the
+        // split's first position), raised only when a row outgrows it by more
+        // than kRescale -- then O and l of that row are rescaled (both halves
+        // take the same decision from the same maximum)
+        float factor = 1.f;
+        bool resc = false;
+        if (t == 0) {
+          m_ref = tmax;
+        } else if (tmax > m_ref + kRescale) {
+          factor = exp2f(m_ref - tmax);
+          m_ref = tmax;
+          resc = true;
+        }
+        if (__any_sync(0xffffffffu, resc)) {   // the warp rescales its half of its 32 rows of O (PV of tile t-1 done)
+          // S(g) was committed after PV(g-2) and PV(g) waits for this tile's P, so
+          // o_done is in phase g-1 or g: the parity wait is unambiguous
+          if (!warp_wait(o_done, (uint32_t)((g - 1) & 1), abort_flag, p.flags)) {
+            ok = false;
+            continue;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 64 * hf; c < 64 * hf + 64; c += 16) {
+            float o16[16];
+            tmem_ld16(o_tm + (uint32_t)c, o16);
+#pragma unroll
+            for (int i2 = 0; i2 < 16; ++i2) o16[i2] *= factor;
+            tmem_st16(o_tm + (uint32_t)c, o16);
+          }
+          tmem_wait_st();
+          l *= factor;
+        }
+        // P = 2^(s - m_ref) <= 2^kRescale as split bf16
+        // (a causal row may see no position of this split: its scores are all
+        // -inf, and so is m_ref; 0 as the reference makes P = 0, l = 0)
+        const float mr = m_ref == -INFINITY ? 0.f : m_ref;
+        uint32_t hi[kUTile / 4], lo[kUTile / 4];
+        float ps = 0.f;
+#pragma unroll
+        for (int i2 = 0; i2 < kUTile / 4; ++i2) {
+          const float p0 = exp2f(s[2 * i2] - mr), p1 = exp2f(s[2 * i2 + 1] - mr);
+          ps += p0 + p1;
+          // hi = p with its low 16 bits cleared (p >= 0: truncation, exact as
+          // bf16), lo = the exact remainder rounded to bf16
+          const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+          hi[i2] = __byte_perm(u0, u1, 0x7632);
+          lo[i2] = pack_bf16x2(p0 - __uint_as_float(u0 & 0xffff0000u), p1 - __uint_as_float(u1 & 0xffff0000u));
+        }
+        l += ps;
+        const int pb = g & 1;
+        if (!warp_wait(&p_free[pb], (uint32_t)((g >> 1) & 1) ^ 1u, abort_flag, p.flags)) {
           ok = false;
           continue;
         }
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = 64 * hf; c < 64 * hf + 64; c += 16) {
-          float o16[16];
-          tmem_ld16(tmem + lane_base + 128u + (uint32_t)c, o16);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) o16[i] *= factor;
-          tmem_st16(tmem + lane_base + 128u + (uint32_t)c, o16);
-        }
-        tmem_wait_st();
-        l *= factor;
+        st_swizzled_half(sP + (size_t)(pb * 2) * kUPPlane, r, 4 * hf, hi);
+        st_swizzled_half(sP + (size_t)(pb * 2 + 1) * kUPPlane, r, 4 * hf, lo);
+        fence_proxy_async_smem();   // generic-proxy P writes -> the tensor core's reads
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[pb]);
       }
-      // P = 2^(s - m_ref) <= 2^kRescale as split bf16
-      // (a causal row may see no position of this split: its scores are all
-      // -inf, and so is m_ref; 0 as the reference makes P = 0, l = 0)
-      const float mr = m_ref == -INFINITY ? 0.f : m_ref;
-      uint32_t hi[kUTile / 4], lo[kUTile / 4];
-      float ps = 0.f;
-#pragma unroll
-      for (int i = 0; i < kUTile / 4; ++i) {
-        const float p0 = exp2f(s[2 * i] - mr), p1 = exp2f(s[2 * i + 1] - mr);
-        ps += p0 + p1;
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
-        hi[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-        lo[i] = pack_bf16x2(p0 - __bfloat162float(h0), p1 - __bfloat162float(h1));
-      }
-      l += ps;
-      const int pb = t & 1;
-      if (!warp_wait(&p_free[pb], (uint32_t)((t >> 1) & 1) ^ 1u, abort_flag, p.flags)) {
-        ok = false;
-        continue;
-      }
-      st_swizzled_half(sP + (size_t)(pb * 2) * kUPPlane, r, 4 * hf, hi);
-      st_swizzled_half(sP + (size_t)(pb * 2 + 1) * kUPPlane, r, 4 * hf, lo);
-      fence_proxy_async_smem();   // generic-proxy P writes -> the tensor core's reads
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[pb]);
-    }
-    // ------------------------------------------------ output: O / l
-    // the row sum from both halves, in half order (both threads get the same
-    // value); every softmax thread meets its partner here on every path
-    xsum[hf * 128 + r] = l;
-    quarter_bar(qq);
-    const float lrow = xsum[r] + xsum[128 + r];
-    if (ok) {
-      const int qd = p.n_q * 128;
-      const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
-      const float lse = lrow > 0.f ? m_ref + log2f(lrow) : -INFINITY;
-      // the last PV has its own barrier: by now o_done may be anywhere between
-      // the last two phases, so a parity wait on it would be ambiguous
-      const bool have = ntiles > 0 && warp_wait(o_final, 0u, abort_flag, p.flags);
-      if (ntiles > 0 && !have) ok = false;
+      // ------------------------------------------------ output: O / l
+      // the row sum from both halves, in half order (both threads get the same
+      // value); every softmax thread meets its partner here on every path
+      float* xs = xsum + (i & 1) * 256;
+      xs[hf * 128 + r] = l;
+      quarter_bar(qq);
+      const float lrow = xs[r] + xs[128 + r];
       if (ok) {
-        tc_fence_after();
-        const int rq = gq * p.R + j;   // row of the merge kernel's layout
-        const size_t prow = (((size_t)(b * p.n_kv + hk) * p.n_splits + split) * p.rows_pad + rq);
-        __nv_bfloat16* orow = p.o + (size_t)(b * p.R + j) * qd + (size_t)(hk * p.G + gq) * 128;
-        {
+        const int qd = p.n_q * 128;
+        const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
+        const float lse = lrow > 0.f ? m_ref + log2f(lrow) : -INFINITY;
+        // the item's last PV has its own barrier: by now o_done may be anywhere
+        // between the last two phases, so a parity wait on it would be ambiguous
+        const bool have = nt > 0 && warp_wait(&o_final[ob], (uint32_t)((mi >> 1) & 1), abort_flag, p.flags);
+        if (nt > 0 && !have) ok = false;
+        if (ok) {
+          tc_fence_after();
+          const int rq = gq * p.R + j;   // row of the merge kernel's layout
+          const size_t prow = ((size_t)pg * p.n_kv + (size_t)hk * S + split) * p.rows_pad + rq;
+          __nv_bfloat16* orow = p.o + (size_t)(b * p.R + j) * qd + (size_t)(hk * p.G + gq) * 128;
           const int h = 64 * hf;   // this half's 64 output columns in one batch of TMEM loads
           float o64[64];
           if (have) {
-            tmem_ld32_issue(tmem + lane_base + 128u + (uint32_t)h, o64);
-            tmem_ld32_issue(tmem + lane_base + 128u + (uint32_t)(h + 32), o64 + 32);
+            tmem_ld32_issue(o_tm + (uint32_t)h, o64);
+            tmem_ld32_issue(o_tm + (uint32_t)(h + 32), o64 + 32);
             tmem_wait_ld();
+            // the buffer is read: the item after next may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_free[ob]);
           } else {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) o64[i] = 0.f;
+            for (int i2 = 0; i2 < 64; ++i2) o64[i2] = 0.f;
           }
           if (rvalid) {
 #pragma unroll
             for (int cc = 0; cc < 64; cc += 16) {
               const float* o16 = o64 + cc;
               const int c = h + cc;
-              if (p.n_splits == 1 && p.o_plane == kF16Plane) {   // one fp16 plane
+              if (S == 1 && p.o_plane == kF16Plane) {   // one fp16 plane
                 uint32_t wh[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  check_f16(o16[2 * i] * inv, p.flags);
-                  check_f16(o16[2 * i + 1] * inv, p.flags);
-                  const __half2 v = __floats2half2_rn(o16[2 * i] * inv, o16[2 * i + 1] * inv);
-                  wh[i] = *reinterpret_cast<const uint32_t*>(&v);
+                for (int i2 = 0; i2 < 8; ++i2) {
+                  check_f16(o16[2 * i2] * inv, p.flags);
+                  check_f16(o16[2 * i2 + 1] * inv, p.flags);
+                  const __half2 v = __floats2half2_rn(o16[2 * i2] * inv, o16[2 * i2 + 1] * inv);
+                  wh[i2] = *reinterpret_cast<const uint32_t*>(&v);
                 }
                 uint4* dh = reinterpret_cast<uint4*>(orow + c);
                 dh[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
                 dh[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
-              } else if (p.n_splits == 1) {   // split bf16: hi plane, lo plane o_plane further
+              } else if (S == 1) {   // split bf16: hi plane, lo plane o_plane further
                 uint32_t wh[8], wl[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i2 = 0; i2 < 8; ++i2) {
                   __nv_bfloat16 h0, l0, h1, l1;
-                  split_bf16(o16[2 * i] * inv, &h0, &l0);
-                  split_bf16(o16[2 * i + 1] * inv, &h1, &l1);
-                  wh[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-                  wl[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                  split_bf16(o16[2 * i2] * inv, &h0, &l0);
+                  split_bf16(o16[2 * i2 + 1] * inv, &h1, &l1);
+                  wh[i2] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                  wl[i2] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
                 }
                 uint4* dh = reinterpret_cast<uint4*>(orow + c);
                 uint4* dl = reinterpret_cast<uint4*>(orow + p.o_plane + c);
@@ -470,15 +698,16 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
               } else {
                 float4* po = reinterpret_cast<float4*>(p.part_o + prow * 128 + c);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  po[i] = make_float4(o16[4 * i] * inv, o16[4 * i + 1] * inv, o16[4 * i + 2] * inv,
-                                      o16[4 * i + 3] * inv);
+                for (int i2 = 0; i2 < 4; ++i2)
+                  po[i2] = make_float4(o16[4 * i2] * inv, o16[4 * i2 + 1] * inv, o16[4 * i2 + 2] * inv,
+                                       o16[4 * i2 + 3] * inv);
               }
             }
           }
+          if (rvalid && S > 1 && hf == 0) p.part_lse[prow] = lse;
         }
-        if (rvalid && p.n_splits > 1 && hf == 0) p.part_lse[prow] = lse;
       }
+      if (nt > 0) ++mi;
     }
   }
 
@@ -488,36 +717,44 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
   }
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag && warp == 8 && lane == 0) {
+  if (*abort_flag && (warp == 8 || warp == 10) && lane == 0) {
     // let every load still in flight land before the shared memory goes away
-    if (q_issued) (void)mbar_wait(q_full, 0u, nullptr);
+    if (q_loads > 0) (void)mbar_wait(q_full, (uint32_t)((q_loads - 1) & 1), nullptr);
+    uint64_t* full = warp == 8 ? k_full : v_full;
     for (int t = max(0, issued - kUStages); t < issued; ++t)
-      (void)mbar_wait(&kv_full[t % kUStages], (uint32_t)((t / kUStages) & 1), nullptr);
+      (void)mbar_wait(&full[t % kUStages], (uint32_t)((t / kUStages) & 1), nullptr);
   }
   if (warp == 9) {
     if (lane == 0) (void)mbar_wait(mma_done, 0u, nullptr);   // MMAs done before TMEM is freed
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, kUTmemCols);
+    tmem_dealloc(tmem, tmem_cols);
   }
 }
 
 }  // namespace
 
 size_t attn_umma_smem_bytes() {
-  return 1024 + 2 * kUQHalf + kUStages * kUStage + 4 * kUPPlane + (1 + 2 * kUStages + 8 + 3) * 8 + 16 +
-         (2 * 2 * 128 + 2 * 128) * sizeof(float);
+  return 1024 + 2 * kUQHalf + kUStages * kUStage + 4 * kUPPlane +
+         (2 + 4 * kUStages + 8 + 1 + 4 + 2 * kUSlots + 1) * 8 + 16 + kUSlots * kUItem * sizeof(int) +
+         (2 * 2 * 128 + 2 * 2 * 128) * sizeof(float);
 }
 
-cudaError_t launch_attention_umma(const AttnUParams& p, int B, cudaStream_t s) {
+cudaError_t launch_attention_umma(const AttnUParams& p, int B, int grid, cudaStream_t s) {
   static bool configured = false;
   const size_t smem = attn_umma_smem_bytes();
   if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(attn_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(attn_umma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_umma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  launch_k(attn_umma_kernel, dim3(p.n_splits, p.n_kv * p.n_qtiles, B), dim3(kUThreads), smem, s, p);
+  const dim3 g = p.work != nullptr ? dim3(grid) : dim3(p.n_splits, p.n_kv * p.n_qtiles, B);
+  if (p.work != nullptr)
+    launch_k(attn_umma_kernel<true>, g, dim3(kUThreads), smem, s, p);
+  else
+    launch_k(attn_umma_kernel<false>, g, dim3(kUThreads), smem, s, p);
   return cudaGetLastError();
 }
 

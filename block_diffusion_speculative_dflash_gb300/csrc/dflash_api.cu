@@ -269,9 +269,15 @@ struct dflash_ctx {
   };
   const TargetRun* trun = nullptr;
   float* d_ulast = nullptr;              // [B][H] input fusion: each sequence's last context feature
-  // attention launch order: sequences by decreasing context length, so the
-  // longest ranges start first (computed on the device at every draft)
-  int32_t* d_seq_order = nullptr;
+  // persistent attention schedule, planned on the device at every draft of a
+  // batch: units [B * 64], per-sequence (S_b, pg_b) [B][2], unit count, one
+  // item counter per layer
+  int32_t* d_plan = nullptr;
+  int32_t *d_work = nullptr, *d_seq_split = nullptr, *d_n_units = nullptr, *d_seq_order = nullptr;
+  uint32_t* d_attn_ctr = nullptr;
+  // the current draft's plan: 0 none, 1 the grid in longest-first order, 2 persistent
+  int plan_mode = 0;
+  int plan_chunk = 0, plan_groups = 0, plan_grid = 0, plan_smax = 0;
   int32_t* d_kseq_in = nullptr;          // [B] staging of a host per-sequence K
   const int32_t* kseq_dev = nullptr;     // the current draft's per-sequence K (device) or null
   int64_t* d_kv_base = nullptr;
@@ -788,8 +794,71 @@ int attn_workspace(dflash_ctx* c, size_t n, float** part_o, float** part_lse, cu
   return DFLASH_OK;
 }
 
-// tcgen05 attention (bf16, head_dim 128): query tiles of 128 rows, about one
-// CTA per SM of at least two 64-position tiles each, then the split merge.
+// Does run_attention take the tcgen05 kernel?
+bool attention_on_umma(const dflash_ctx* c) {
+  const dflash_config& g = c->cfg;
+  return c->bf16 && c->d == 128 && (c->attn_umma || c->target) && 128 % (g.n_q_heads / g.n_kv_heads) == 0;
+}
+
+// Work items of the persistent attention per SM: enough for the longest-first
+// order to even out the SMs' loads, few enough that each item streams several
+// tiles.
+constexpr int kAttnItemsPerSm = 1;
+// Batches from this size take the persistent attention; smaller ones one CTA
+// per (split, head, sequence) in longest-first order.
+constexpr int kAttnPersistentMinBatch = 16;
+
+// The attention schedule of a batch's draft with R block rows per sequence:
+// the host's upper bounds of the contexts give the tiles per split (chunk),
+// the partial groups to provide and the grid; the device plans with the live
+// lengths (launch_attn_plan) once, for every layer.
+int plan_attention(dflash_ctx* c, int R, cudaStream_t s) {
+  const dflash_config& g = c->cfg;
+  const int G = g.n_q_heads / g.n_kv_heads;
+  const int n_qtiles = (R + 128 / G - 1) / (128 / G);
+  const int rows_pad = n_qtiles * 128;
+  const int64_t n_hq = (int64_t)g.n_kv_heads * n_qtiles;
+  int64_t tiles_total = 0;
+  for (int b = 0; b < c->B; ++b) tiles_total += (ctx_keys_ub(c, b) + R + 63) / 64;
+  const int64_t items = (int64_t)kAttnItemsPerSm * c->num_sms;
+  const int chunk = (int)std::max<int64_t>(2, (tiles_total * n_hq + items - 1) / items);
+  const int s_max = 64;
+  int64_t groups_ub = 0, units_ub = 0;
+  int s_ub = 1;
+  for (int b = 0; b < c->B; ++b) {
+    const int64_t tb = (ctx_keys_ub(c, b) + R + 63) / 64;
+    const int sb = (int)std::min<int64_t>(s_max, std::max<int64_t>(1, (tb + chunk - 1) / chunk));
+    units_ub += sb;
+    if (sb > 1) groups_ub += sb;
+    s_ub = std::max(s_ub, sb);
+  }
+  const size_t group_floats = (size_t)g.n_kv_heads * rows_pad * 129;
+  int64_t max_groups = 0;   // 0: every sequence in one split, no partials and no merge
+  if (groups_ub > 0) {
+    if (c->attn_scratch_ext != nullptr) {
+      max_groups = (int64_t)(c->attn_scratch_ext_floats / group_floats);
+      if (max_groups < 2) max_groups = 0;
+    } else {
+      max_groups = 2 * groups_ub;   // room for the contexts to grow under a recorded draft
+    }
+  }
+  c->plan_groups = (int)std::min<int64_t>(max_groups, 1 << 30);
+  c->plan_smax = max_groups > 0 ? s_ub : 1;
+  c->plan_grid = (int)std::max<int64_t>(1, std::min<int64_t>(c->num_sms, units_ub * n_hq));
+  c->plan_chunk = chunk;
+  launch_attn_plan(c->st, c->B, chunk, s_max, c->plan_groups, c->d_work, c->d_seq_split, c->d_n_units,
+                   c->d_seq_order, c->d_attn_ctr, c->nl, s);
+  CK(cudaGetLastError());
+  c->launches += 1;
+  c->plan_mode = c->B >= kAttnPersistentMinBatch ? 2 : 1;
+  return DFLASH_OK;
+}
+
+// tcgen05 attention (bf16, head_dim 128): query tiles of 128 rows.  With a
+// draft's plan (a batch), the persistent kernel works through the planned
+// items; otherwise (one sequence, or the target's forward) one CTA per
+// (split, head x query tile, sequence) with about one CTA per SM of at least
+// two 64-position tiles.  Then the split merge.
 int run_attention_umma(dflash_ctx* c, const void* qb, void* ob, int l, int R, cudaStream_t s) {
   const dflash_config& g = c->cfg;
   AttnUParams p;
@@ -818,6 +887,26 @@ int run_attention_umma(dflash_ctx* c, const void* qb, void* ob, int l, int R, cu
   p.n_kv = g.n_kv_heads;
   p.n_qtiles = (R + p.JT - 1) / p.JT;
   p.rows_pad = p.n_qtiles * 128;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->d));
+  p.flags = c->d_flags;
+  p.o_plane = c->op16_now ? kF16Plane : (size_t)M * c->q_dim;
+  p.causal = c->target ? 1 : 0;
+  if (c->plan_mode == 2) {
+    p.work = c->d_work;
+    p.seq_split = c->d_seq_split;
+    p.n_units = c->d_n_units;
+    p.item_ctr = c->d_attn_ctr + l;
+    if (c->plan_groups > 0)
+      RET(attn_workspace(c, (size_t)c->plan_groups * p.n_kv * p.rows_pad, &p.part_o, &p.part_lse, s));
+    CK(launch_attention_umma(p, c->B, c->plan_grid, s));
+    c->launches += 1;
+    if (c->plan_groups > 0) {
+      CK(launch_attn_merge(p.part_o, p.part_lse, p.n_kv, c->plan_smax, p.G * R, p.rows_pad, R, p.G, p.n_q, p.o,
+                           p.o_plane, c->B, s, c->d_flags, c->d_seq_split));
+      c->launches += 1;
+    }
+    return DFLASH_OK;
+  }
   int64_t tiles_total = 0;
   int max_tiles = 1;
   for (int b = 0; b < c->B; ++b) {
@@ -829,14 +918,10 @@ int run_attention_umma(dflash_ctx* c, const void* qb, void* ob, int l, int R, cu
   const int64_t per_cta = std::max<int64_t>(2, (tiles_total + c->num_sms - 1) / c->num_sms);
   p.n_splits = (int)std::max<int64_t>(1, std::min<int64_t>(64, (max_tiles + per_cta - 1) / per_cta));
   p.n_splits = clamp_splits_to_scratch(c, p.n_splits, (size_t)c->B * p.n_kv * p.rows_pad);
-  if (c->B > 1) p.seq_order = c->d_seq_order;   // longest contexts first (ordered once per draft)
+  if (c->plan_mode == 1) p.seq_order = c->d_seq_order;   // longest contexts first
   if (p.n_splits > 1)
     RET(attn_workspace(c, (size_t)c->B * p.n_kv * p.n_splits * p.rows_pad, &p.part_o, &p.part_lse, s));
-  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->d));
-  p.flags = c->d_flags;
-  p.o_plane = c->op16_now ? kF16Plane : (size_t)M * c->q_dim;
-  p.causal = c->target ? 1 : 0;
-  CK(launch_attention_umma(p, c->B, s));
+  CK(launch_attention_umma(p, c->B, 0, s));
   c->launches += 1;
   if (p.n_splits > 1) {
     CK(launch_attn_merge(p.part_o, p.part_lse, p.n_kv, p.n_splits, p.G * R, p.rows_pad, R, p.G, p.n_q,
@@ -856,9 +941,8 @@ int run_attention(dflash_ctx* c, const T* qb, T* ob, int l, int R, cudaStream_t 
     c->launches += 1;
     return DFLASH_OK;
   }
-  const int G = g.n_q_heads / g.n_kv_heads;
   // (the target's causal mask is in the tcgen05 kernel and the generic one)
-  if ((c->attn_umma || c->target) && 128 % G == 0) return run_attention_umma(c, qb, ob, l, R, s);
+  if (attention_on_umma(c)) return run_attention_umma(c, qb, ob, l, R, s);
   AttnTcParams p;
   memset(&p, 0, sizeof(p));
   p.tm_kv = c->tm_kv;
@@ -1062,10 +1146,12 @@ int draft_bf16(dflash_ctx* c, const int32_t* anchor_dev, int K, float* logits_de
                         op16 ? kF16Plane : (size_t)M * H, c->d_flags, c->kseq_dev, s,
                         c->trun ? c->trun->tokens : nullptr);
   c->launches += 1;
-  if (B > 1) {   // the attention's launch order: longest context first
-    launch_seq_order(c->st, B, c->d_seq_order, s);
-    c->launches += 1;
-  }
+  struct PlanScope {
+    dflash_ctx* c;
+    ~PlanScope() { c->plan_mode = 0; }
+  } plan_scope{c};
+  // a batch's attention: one persistent schedule for every layer
+  if (B > 1 && B <= attn_plan_max_batch() && attention_on_umma(c)) RET(plan_attention(c, R, s));
   const int n_ss = H / kTileRows;
   // a pending append's K/V are projected with the layers' QKV when both fit
   // one token tile each, else on their own first
@@ -1396,7 +1482,7 @@ void free_ctx(dflash_ctx* c) {
   for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
   void* ptrs[] = {c->d_i32, c->d_kv_base, c->d_flags, c->d_draft, c->d_targets, c->d_rope, c->arena_raw, c->h,
                   c->xn, c->qb, c->ob, c->ab, c->xf, c->ws, c->stage, c->ub, c->attn_ws, c->d_keys,
-                  c->d_counters, c->d_ss, c->ybuf, c->d_ss_ctx, c->d_ulast, c->d_seq_order, c->w16};
+                  c->d_counters, c->d_ss, c->ybuf, c->d_ss_ctx, c->d_ulast, c->d_plan, c->w16};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   cudaGetLastError();
@@ -1562,8 +1648,13 @@ static int create_impl(const dflash_config* cfg, const dflash_weights* w, int32_
       !dalloc((void**)&c->d_counters, sizeof(unsigned int) * kCounters) ||
       !dalloc((void**)&c->d_ss_ctx, sizeof(float) * (size_t)(c->H / kTileRows + 1) * 128) ||
       (g.conditioning == DFLASH_COND_INPUT && !dalloc((void**)&c->d_ulast, sizeof(float) * (size_t)B * c->H)) ||
-      !dalloc((void**)&c->d_seq_order, sizeof(int32_t) * (size_t)B))
+      !dalloc((void**)&c->d_plan, sizeof(int32_t) * ((size_t)B * (64 + 3) + 1 + (size_t)c->nl)))
     return bail(fail(DFLASH_ERR_OOM, "state allocation failed"));
+  c->d_work = c->d_plan;
+  c->d_seq_split = c->d_work + (size_t)B * 64;
+  c->d_seq_order = c->d_seq_split + 2 * (size_t)B;
+  c->d_n_units = c->d_seq_order + (size_t)B;
+  c->d_attn_ctr = reinterpret_cast<uint32_t*>(c->d_n_units + 1);
   c->cond = g.conditioning;
   if (c->d_ulast && cudaMemset(c->d_ulast, 0, sizeof(float) * (size_t)B * c->H) != cudaSuccess)
     return bail(fail(DFLASH_ERR_CUDA, "state initialisation failed"));

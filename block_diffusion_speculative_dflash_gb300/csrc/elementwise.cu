@@ -809,23 +809,113 @@ void launch_rows_prep(const int32_t* rows_in, int rows_max, int B, int32_t* rows
 void launch_mask_drafts(int32_t* drafts, SeqState st, int B, int K, cudaStream_t s) {
   launch_k(mask_drafts_kernel, dim3((B * K + 255) / 256), dim3(256), 0, s, drafts, st, B, K);
 }
-// order[rank] = b, sequences by decreasing block_base (the context the block
-// attends to), ties by index: rank = #{longer} + #{equal with a lower index}.
-__global__ void seq_order_kernel(SeqState st, int B, int32_t* __restrict__ order) {
+// Sum of v over the CTA (every thread gets it); red holds 32 ints.
+__device__ int block_sum_int(int v, int* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();   // red is free (a previous sum has been read)
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int t = 0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+  return t;
+}
+
+// The attention schedule of one draft (one CTA).  Sequence b
+// attends over L_b = its context + its K_b + 1 block rows (capped by its
+// capacity): T_b = ceil(L_b / 64) tiles, S_b = min(s_max, ceil(T_b / c)) KV
+// splits, reduced so that none is empty, with c = chunk grown by a quarter
+// until the partial groups of the multi-split sequences fit max_groups.  Units
+// (b, split) are listed sequence by sequence in decreasing tiles per split
+// (ties by index), so that the longest items start first; a multi-split
+// sequence's partials take groups pg_b .. pg_b + S_b - 1 in that order.
+// order[k]: the sequence of rank k by decreasing context length (ties by
+// index), the launch order of the one-item-per-CTA attention grid.
+constexpr int kPlanMaxB = 2048;
+__global__ void __launch_bounds__(256) attn_plan_kernel(SeqState st, int B, int chunk, int s_max, int max_groups,
+                                                        int32_t* __restrict__ work, int32_t* __restrict__ seq_split,
+                                                        int32_t* __restrict__ n_units, int32_t* __restrict__ order_out,
+                                                        uint32_t* __restrict__ ctrs, int n_ctrs) {
   pdl_trigger();
   pdl_wait();
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= B) return;
-  const int mine = block_base(st, b);
-  int rank = 0;
-  for (int o = 0; o < B; ++o) {
-    const int other = block_base(st, o);
-    rank += (other > mine || (other == mine && o < b)) ? 1 : 0;
+  extern __shared__ int plan_sm[];
+  int* T = plan_sm;      // [B] tiles
+  int* S = T + B;        // [B] splits
+  int* order = S + B;    // [B] sequence of each rank
+  int* start = order + B;   // [B] first unit of each rank
+  __shared__ int red[32];
+  const int tid = threadIdx.x, nth = blockDim.x;
+  for (int b = tid; b < B; b += nth) {
+    const int L = min(block_base(st, b) + st.rblk[b], st.cap[b]);
+    T[b] = (L + 63) / 64;
   }
-  order[rank] = b;
+  for (int i = tid; i < n_ctrs; i += nth) ctrs[i] = 0u;
+  __syncthreads();
+  int c = max(1, chunk);
+  for (int iter = 0;; ++iter) {
+    int part = 0;
+    for (int b = tid; b < B; b += nth) {
+      const int sb = min(s_max, max(1, (T[b] + c - 1) / c));
+      part += sb > 1 ? sb : 0;
+    }
+    if (block_sum_int(part, red) <= max_groups) break;
+    if (iter >= 200 || c >= (1 << 28)) {   // every sequence in one split (no partials)
+      c = 1 << 30;
+      break;
+    }
+    c += (c >> 2) + 1;
+  }
+  for (int b = tid; b < B; b += nth) {
+    int sb = min(s_max, max(1, (T[b] + c - 1) / c));
+    if (T[b] > 0) {
+      const int per = (T[b] + sb - 1) / sb;
+      sb = (T[b] + per - 1) / per;
+    }
+    S[b] = sb;
+  }
+  __syncthreads();
+  for (int b = tid; b < B; b += nth) {   // launch order of the grid: context length
+    const int mine = block_base(st, b);
+    int rank = 0;
+    for (int o = 0; o < B; ++o) {
+      const int other = block_base(st, o);
+      rank += (other > mine || (other == mine && o < b)) ? 1 : 0;
+    }
+    order_out[rank] = b;
+  }
+  for (int b = tid; b < B; b += nth) {
+    const int mine = (T[b] + S[b] - 1) / S[b];
+    int rank = 0;
+    for (int o = 0; o < B; ++o) {
+      const int other = (T[o] + S[o] - 1) / S[o];
+      rank += (other > mine || (other == mine && o < b)) ? 1 : 0;
+    }
+    order[rank] = b;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int u = 0, pg = 0;
+    for (int k = 0; k < B; ++k) {
+      const int b = order[k], sb = S[b];
+      start[k] = u;
+      seq_split[2 * b] = sb;
+      seq_split[2 * b + 1] = sb > 1 ? pg : 0;
+      u += sb;
+      pg += sb > 1 ? sb : 0;
+    }
+    *n_units = u;
+  }
+  __syncthreads();
+  for (int k = tid; k < B; k += nth) {
+    const int b = order[k];
+    for (int sp = 0; sp < S[b]; ++sp) work[start[k] + sp] = (b << 8) | sp;
+  }
 }
-void launch_seq_order(SeqState st, int B, int32_t* order, cudaStream_t s) {
-  launch_k(seq_order_kernel, dim3((B + 127) / 128), dim3(128), 0, s, st, B, order);
+int attn_plan_max_batch() { return kPlanMaxB; }
+void launch_attn_plan(SeqState st, int B, int chunk, int s_max, int max_groups, int32_t* work, int32_t* seq_split,
+                      int32_t* n_units, int32_t* order, uint32_t* ctrs, int n_ctrs, cudaStream_t s) {
+  launch_k(attn_plan_kernel, dim3(1), dim3(256), sizeof(int) * 4 * (size_t)B, s, st, B, chunk, s_max, max_groups,
+           work, seq_split, n_units, order, ctrs, n_ctrs);
 }
 
 void launch_append_commit(const int32_t* rows, SeqState st, int B, cudaStream_t s) {

@@ -189,23 +189,43 @@ struct AttnUParams {
   CUtensorMap tm_kv;            // KV arena as [rows, 128] bf16, 64 x 64 boxes, 128-byte swizzle
   CUtensorMap tm_q;             // rotated queries, 3-D view, 128-byte swizzle
   __nv_bfloat16* o;             // split bf16 [2][M][n_q * 128]
-  float* part_o;                // [B, n_kv, n_splits, rows_pad, 128] (n_splits > 1)
-  float* part_lse;              // [B, n_kv, n_splits, rows_pad], log2 domain
+  // partials of sequence b (S_b > 1 splits, first partial group pg_b): row
+  // ((pg_b * n_kv + hk * S_b) + split) * rows_pad + rq of [groups * n_kv * rows_pad][128]
+  float* part_o;
+  float* part_lse;              // [groups * n_kv * rows_pad], log2 domain
   SeqState st;
   KvArena kv;
   int layer, R, n_q, n_kv, G, JT;
-  int rows_pad, n_qtiles, n_splits;
+  int rows_pad, n_qtiles;
+  int n_splits;                 // grid mode: every sequence's split count (pg_b = b * n_splits)
   int causal;                   // 1: block row j sees positions <= block_base + j only
-  const int32_t* seq_order;     // sequence of grid row z (longest context first), or null: z
+  const int32_t* seq_order;     // grid mode: sequence of grid row z (longest context first), or null: z
+  // persistent schedule (null work: grid mode, one item per CTA)
+  const int32_t* work;          // units (b << 8 | split) in processing order
+  const int32_t* seq_split;     // [B][2]: S_b, pg_b
+  const int32_t* n_units;       // number of units
+  uint32_t* item_ctr;           // this launch's item counter (zero at launch)
   float scale_log2;
   uint32_t* flags;
   size_t o_plane;
 };
 size_t attn_umma_smem_bytes();
-cudaError_t launch_attention_umma(const AttnUParams& p, int B, cudaStream_t s);
+cudaError_t launch_attention_umma(const AttnUParams& p, int B, int grid, cudaStream_t s);
+// seq_split null: every sequence has S splits, partial group b * S; else the
+// per-sequence S_b and pg_b of the persistent schedule (S the largest expected,
+// sequences with one split are skipped: their output is written directly)
 cudaError_t launch_attn_merge(const float* part_o, const float* part_lse, int n_kv, int S, int rows, int rows_pad,
                               int R, int G, int n_q, __nv_bfloat16* o, size_t o_plane, int B, cudaStream_t s,
-                              uint32_t* flags);
+                              uint32_t* flags, const int32_t* seq_split = nullptr);
+// The attention schedule of one draft (all layers): order[k] = the sequence of
+// rank k by decreasing context (ties by index); for the persistent kernel, per sequence b,
+// T_b = ceil(L_b / 64) tiles of the live length L_b, S_b = ceil(T_b / c) KV
+// splits (at most s_max, none empty) with c >= chunk grown until the splits of
+// multi-split sequences fit max_groups partial groups; units (b, split) ordered
+// by tiles per split, most first; the per-layer item counters zeroed.
+void launch_attn_plan(SeqState st, int B, int chunk, int s_max, int max_groups, int32_t* work, int32_t* seq_split,
+                      int32_t* n_units, int32_t* order, uint32_t* ctrs, int n_ctrs, cudaStream_t s);
+int attn_plan_max_batch();   // largest batch one plan CTA takes (shared-memory tables)
 size_t attn_tc_smem_bytes();
 cudaError_t launch_attention_tc(const AttnTcParams& p, int n_consumer_warps, int B, cudaStream_t s);
 void launch_argmax_finalize(unsigned long long* keys, int rows, int32_t* ids, cudaStream_t s);
@@ -250,7 +270,6 @@ void launch_rows_prep(const int32_t* rows_in, int rows_max, int B, int32_t* rows
                       cudaStream_t s);
 void launch_mask_drafts(int32_t* drafts, SeqState st, int B, int K, cudaStream_t s);
 void launch_append_commit(const int32_t* rows, SeqState st, int B, cudaStream_t s);
-void launch_seq_order(SeqState st, int B, int32_t* order, cudaStream_t s);
 template <typename T>
 void launch_ulast(const T* u, size_t lo_plane, const float* ss, int n_ss, int ss_ld, int t0, int Mc,
                   const int32_t* rows, int rows_max, int B, int H, float eps, float* u_last, cudaStream_t s);
