@@ -80,9 +80,13 @@ def test_tiny_bf16_loop(torch_cuda):
     (15, [2048], 8, 2),                 # one query tile, many KV splits
     (40, [1, 300, 5000], 4, 1),         # G*R = 164 rows -> two query tiles; ragged batch
     (7, [63, 64, 65, 129], 16, 8),      # tile-boundary contexts, GQA group 2
+    # 16+ sequences: the persistent kernel on the device-planned schedule (per-sequence
+    # splits, one-split sequences written directly, the rest merged)
+    (15, [1, 2, 63, 64, 65, 127, 128, 129, 300, 700, 1000, 1500, 2047, 2048, 3000, 4097, 5000, 9000], 8, 2),
+    (40, [5000, 1, 64, 300, 2100, 17, 900, 129, 63, 4000, 2, 1200, 700, 65, 3333, 128], 4, 1),   # two query tiles
 ])
 def test_tensor_core_attention_shapes(torch_cuda, K, ctx, n_q, n_kv):
-    """bf16, head_dim 128: the TMA + mma.sync attention (split-KV and merge) against the oracle."""
+    """bf16, head_dim 128: the tensor-core attention (split-KV and merge) against the oracle."""
     s = CONFIGS["tiny_f32"].with_(dtype="bf16", head_dim=128, n_q_heads=n_q, n_kv_heads=n_kv, hidden=256,
                                   n_layers=2, batch=len(ctx), K=K, K_max=K, seed=21)
     Wn = make_weights(s)

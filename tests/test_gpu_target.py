@@ -23,13 +23,17 @@ def _shape(**kw):
     return CONFIGS["tiny_f32"].with_(**{**dict(dtype="bf16", head_dim=128, n_layers=2, seed=48), **kw})
 
 
-@pytest.mark.parametrize("shape_kw", [dict(), dict(n_layers=3, n_q_heads=8, n_kv_heads=2)])
-def test_target_forward_matches_oracle(shape_kw):
+@pytest.mark.parametrize("shape_kw,B", [
+    (dict(), 3),
+    (dict(n_layers=3, n_q_heads=8, n_kv_heads=2), 3),
+    (dict(n_q_heads=8, n_kv_heads=2), 17),   # 16+ sequences: the persistent causal attention
+])
+def test_target_forward_matches_oracle(shape_kw, B):
     torch = _cuda()
     from block_diffusion_speculative_dflash_gb300 import DFlashTarget, TargetConfig
     s = _shape(**shape_kw)
     W = make_weights(s)
-    B, r_max = 3, 64
+    r_max = 64
     feat = [0, s.n_layers - 1]
     tg = DFlashTarget(TargetConfig.from_shape(s, r_max, feat_layers=feat), upload_weights(W), B)
     orc = OracleTarget(s, W, B, feat_layers=feat)
@@ -44,6 +48,7 @@ def test_target_forward_matches_oracle(shape_kw):
         tg.forward(to_device(toks), ids, logits=z, feats=f)
         torch.cuda.synchronize()
         ig, zg, fg = ids.cpu().numpy(), z.cpu().numpy(), f.float().cpu().numpy()
+        compared = 0
         for b in range(B):
             io, zo, fo = orc.forward(b, toks[b])
             err = row_rel_err(zg[b], zo)
@@ -51,15 +56,16 @@ def test_target_forward_matches_oracle(shape_kw):
             assert np.array_equal(ig[b], greedy_ids(zg[b])), "fused argmax != argmax(logits)"
             row_err = np.max(np.abs(zg[b] - zo), axis=-1)
             ok = top2_gap(zo) > np.maximum(1e-2, 2.0 * row_err)
-            assert ok.sum() > 0
+            compared += int(ok.sum())
             assert np.array_equal(ig[b][ok], io[ok]), f"seq {b} R {R}: ids differ where the gap decides"
             ferr = row_rel_err(fg[b], fo)
             assert ferr.max() <= rtol, f"seq {b} R {R}: features rel err {ferr.max():.3e}"
             orc.commit(b, int(keep[b]))
+        assert compared > 0   # (a single-row block of one sequence may have no decidable row)
         tg.commit(to_device(keep.astype(np.int32)) if device_keep else keep.astype(np.int32))
         np.testing.assert_array_equal(tg.query(), np.array(orc.len, np.int32))
 
-    run(37, np.array([37, 5, 20]))                 # prefill, kept to ragged lengths
+    run(37, np.resize(np.array([37, 5, 20, 1, 30, 12]), B))   # prefill, kept to ragged lengths
     for it, R in enumerate([17, 11, 40, 3, 1, 60]):   # verify blocks (60 rows: 180 GEMM rows, plain bf16 operands)
         run(R, rng.integers(1, R + 1, size=B), device_keep=it % 2 == 1)
 
