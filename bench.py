@@ -207,7 +207,8 @@ def cpu_oracle_run(s, K, steps, warmup, seq_limit=None, conditioning="kv"):
         if t >= warmup:
             times.append(time.perf_counter() - t0)
     sample = (f"{B} of {s.batch} sequence(s) of the workload, {steps} full iterations "
-              f"(draft + verify + append) after {warmup} warm-up, oracle in fp32")
+              f"(draft + verify + append) after {warmup} warm-up, oracle in fp32; the GPU `value` times "
+              f"draft + verify without the append, its `iteration` figure includes it")
     return float(np.mean(times)), sample, cores, B
 
 
