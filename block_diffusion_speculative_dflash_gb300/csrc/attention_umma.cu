@@ -102,29 +102,35 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16_bmn(int M, int N) {
   return umma_idesc_bf16(M, N) | (1u << 16);
 }
 
-// Half a row (chunks c0 .. c0 + 3, 32 bf16) of row r of a K-major,
-// 128-byte-swizzled tile whose base is 1024-B aligned: chunk c of row r sits
-// at chunk c ^ (r & 7).
-__device__ __forceinline__ void st_swizzled_half(uint8_t* tile, int r, int c0, const uint32_t (&w)[16]) {
+// NW / 4 chunks of 16 bytes (c0 ..) of row r of a K-major, 128-byte-swizzled
+// tile whose base is 1024-B aligned: chunk c of row r sits at chunk c ^ (r & 7).
+template <int NW>
+__device__ __forceinline__ void st_swizzled_part(uint8_t* tile, int r, int c0, const uint32_t (&w)[NW]) {
   uint8_t* row = tile + (size_t)r * 128;
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
+  for (int c = 0; c < NW / 4; ++c)
     *reinterpret_cast<uint4*>(row + (((c0 + c) ^ (r & 7)) << 4)) =
         make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 }
 
-// The two softmax warps of TMEM lane quarter q (w and w + 4) meet on named
-// barrier 1 + q; the _and form also returns whether v held in all 64 threads,
-// so that both warps leave the tile loop on the same tile and meet the same
-// number of times on every path.
-__device__ __forceinline__ void quarter_bar(int q) { asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory"); }
+// Threads per query row of the softmax: a row's tile of 64 positions and its
+// 128 output dimensions are split between kParts warps of one TMEM lane quarter
+// (warps w, w + 4, ..), which meet on named barrier 1 + q; the _and form also
+// returns whether v held in all of them, so that they leave the tile loop on
+// the same tile and meet the same number of times on every path.
+constexpr int kParts = 2;
+constexpr int kPCols = kUTile / kParts;    // score positions per thread
+constexpr int kODims = 128 / kParts;       // output dimensions per thread
+__device__ __forceinline__ void quarter_bar(int q) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + q), "n"(32 * kParts) : "memory");
+}
 __device__ __forceinline__ bool quarter_bar_and(int q, bool v) {
   uint32_t all;
   asm volatile(
-      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, 64, pi;\n\t"
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, %3, pi;\n\t"
       "selp.u32 %0, 1, 0, po;\n\t}"
       : "=r"(all)
-      : "r"((uint32_t)v), "r"(1 + q)
+      : "r"((uint32_t)v), "r"(1 + q), "n"(32 * kParts)
       : "memory");
   return all != 0;
 }
@@ -148,7 +154,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return okv != 0;
 }
 
-constexpr int kUThreads = 352;   // 8 softmax warps, the query/K producer, the MMA issuer, the V producer
+constexpr int kSoftWarps = 4 * kParts;
+constexpr int kWarpQK = kSoftWarps, kWarpMma = kSoftWarps + 1, kWarpV = kSoftWarps + 2;
+constexpr int kUThreads = 32 * (kSoftWarps + 3);   // softmax warps, the query/K producer, the MMA issuer, the V producer
 constexpr int kUSlots = 4;       // work items published ahead of the consumers
 constexpr int kUItem = 10;       // ints per published item
 
@@ -245,7 +253,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
   int* items = reinterpret_cast<int*>(tmem_slot + 4);           // [kUSlots][kUItem]
   // the two halves' tile maxima [tile parity][half][row] and row sums [item parity][half][row]
   float* xmax = reinterpret_cast<float*>(items + kUSlots * kUItem);
-  float* xsum = xmax + 2 * 2 * 128;
+  float* xsum = xmax + 2 * kParts * 128;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -259,15 +267,15 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 8);
-      mbar_init(&p_full[i], 8);
+      mbar_init(&s_free[i], kSoftWarps);
+      mbar_init(&p_full[i], kSoftWarps);
       mbar_init(&p_free[i], 1);
       mbar_init(&o_final[i], 1);
-      mbar_init(&o_free[i], 8);
+      mbar_init(&o_free[i], kSoftWarps);
     }
     for (int i = 0; i < kUSlots; ++i) {
       mbar_init(&it_full[i], 1);
-      mbar_init(&it_free[i], 10);   // eight softmax warps, the MMA issuer and the V producer
+      mbar_init(&it_free[i], kSoftWarps + 2);   // the softmax warps, the MMA issuer and the V producer
     }
     mbar_init(o_done, 1);
     mbar_init(mma_done, 1);
@@ -276,7 +284,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
   }
   constexpr bool grid_mode = !PERSIST;
   const uint32_t tmem_cols = grid_mode ? kUTmemCols / 2 : kUTmemCols;
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tmem_alloc(tmem_slot, tmem_cols);
     tmem_relinquish();
   }
@@ -295,7 +303,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
   if constexpr (grid_mode) gx = decode_item<true>(p, 0);
   bool ok = true;
   int issued = 0, q_loads = 0;   // producers: K (or V) tiles and query tiles whose loads were issued
-  if (warp == 8) {
+  if (warp == kWarpQK) {
     // ------------------------------------------------ queries and K
     if (lane == 0) {
       const int n_items = grid_mode ? 1 : *p.n_units * p.n_kv * p.n_qtiles;
@@ -365,7 +373,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
         if (!ok) break;
       }
     }
-  } else if (warp == 10) {
+  } else if (warp == kWarpV) {
     // ------------------------------------------------ V
     if (lane == 0) {
       for (int i = 0;; ++i) {
@@ -402,7 +410,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
         if (!ok) break;
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_s = umma_idesc_bf16(128, kUTile);
@@ -500,7 +508,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
   } else {
     // ------------------------------------------------ softmax, two threads per query row
     const int r = threadIdx.x & 127;                    // TMEM lane = tile row
-    const int hf = threadIdx.x >> 7;                    // half: positions 32 hf .. of a tile, dims 64 hf ..
+    const int hf = threadIdx.x >> 7;                    // part: positions kPCols hf .. of a tile, dims kODims hf ..
     const int qq = warp & 3;                            // TMEM lane quarter
     const uint32_t lane_base = (uint32_t)(qq * 32) << 16;
     int g = 0, mi = 0;   // K/V tiles and items with tiles so far
@@ -537,21 +545,24 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
       // together at the next meeting
       for (int t = 0; t < nt; ++t, ++g) {
         const int sb = g & 1;
-        float s[kUTile / 2];
+        float s[kPCols];
         float hmax = -INFINITY;
         if (ok && warp_wait(&s_full[sb], (uint32_t)((g >> 1) & 1), abort_flag, p.flags)) {
           tc_fence_after();
-          tmem_ld32_issue(tmem + lane_base + (uint32_t)(sb * kUTile + 32 * hf), s);
+          if constexpr (kPCols == 32)
+            tmem_ld32_issue(tmem + lane_base + (uint32_t)(sb * kUTile + kPCols * hf), s);
+          else
+            tmem_ld16(tmem + lane_base + (uint32_t)(sb * kUTile + kPCols * hf), s);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&s_free[sb]);
           // scale into the log2 domain; positions past the split (and, causal,
           // past the row's own position) are masked
-          const int pos0 = p_begin + t * kUTile + 32 * hf;
+          const int pos0 = p_begin + t * kUTile + kPCols * hf;
           const int p_row = p.causal ? min(p_end, row_lim + 1) : p_end;
 #pragma unroll
-          for (int i2 = 0; i2 < kUTile / 2; ++i2) {
+          for (int i2 = 0; i2 < kPCols; ++i2) {
             const float v = pos0 + i2 < p_row ? s[i2] * p.scale_log2 : -INFINITY;
             s[i2] = v;
             hmax = fmaxf(hmax, v);
@@ -561,12 +572,14 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
         }
         // the row's maximum over the whole tile: this half's and the partner's
         // (double-buffered by tile parity, so one meeting per tile suffices)
-        xmax[(sb * 2 + hf) * 128 + r] = hmax;
+        xmax[(sb * kParts + hf) * 128 + r] = hmax;
         if (!quarter_bar_and(qq, ok)) {
           ok = false;
           break;
         }
-        const float tmax = fmaxf(hmax, xmax[(sb * 2 + (hf ^ 1)) * 128 + r]);
+        float tmax = xmax[(sb * kParts) * 128 + r];
+#pragma unroll
+        for (int q2 = 1; q2 < kParts; ++q2) tmax = fmaxf(tmax, xmax[(sb * kParts + q2) * 128 + r]);
         // reference maximum: set by the first tile (which always holds the
         // split's first position), raised only when a row outgrows it by more
         // than kRescale -- then O and l of that row are rescaled (both halves
@@ -589,7 +602,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
           }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 64 * hf; c < 64 * hf + 64; c += 16) {
+          for (int c = kODims * hf; c < kODims * hf + kODims; c += 16) {
             float o16[16];
             tmem_ld16(o_tm + (uint32_t)c, o16);
 #pragma unroll
@@ -603,10 +616,10 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
         // (a causal row may see no position of this split: its scores are all
         // -inf, and so is m_ref; 0 as the reference makes P = 0, l = 0)
         const float mr = m_ref == -INFINITY ? 0.f : m_ref;
-        uint32_t hi[kUTile / 4], lo[kUTile / 4];
+        uint32_t hi[kPCols / 2], lo[kPCols / 2];
         float ps = 0.f;
 #pragma unroll
-        for (int i2 = 0; i2 < kUTile / 4; ++i2) {
+        for (int i2 = 0; i2 < kPCols / 2; ++i2) {
           const float p0 = exp2f(s[2 * i2] - mr), p1 = exp2f(s[2 * i2 + 1] - mr);
           ps += p0 + p1;
           // hi = p with its low 16 bits cleared (p >= 0: truncation, exact as
@@ -621,8 +634,8 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
           ok = false;
           continue;
         }
-        st_swizzled_half(sP + (size_t)(pb * 2) * kUPPlane, r, 4 * hf, hi);
-        st_swizzled_half(sP + (size_t)(pb * 2 + 1) * kUPPlane, r, 4 * hf, lo);
+        st_swizzled_part(sP + (size_t)(pb * 2) * kUPPlane, r, (kPCols / 8) * hf, hi);
+        st_swizzled_part(sP + (size_t)(pb * 2 + 1) * kUPPlane, r, (kPCols / 8) * hf, lo);
         fence_proxy_async_smem();   // generic-proxy P writes -> the tensor core's reads
         tc_fence_before();
         __syncwarp();
@@ -631,10 +644,12 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
       // ------------------------------------------------ output: O / l
       // the row sum from both halves, in half order (both threads get the same
       // value); every softmax thread meets its partner here on every path
-      float* xs = xsum + (i & 1) * 256;
+      float* xs = xsum + (i & 1) * kParts * 128;
       xs[hf * 128 + r] = l;
       quarter_bar(qq);
-      const float lrow = xs[r] + xs[128 + r];
+      float lrow = xs[r];
+#pragma unroll
+      for (int q2 = 1; q2 < kParts; ++q2) lrow += xs[q2 * 128 + r];
       if (ok) {
         const int qd = p.n_q * 128;
         const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
@@ -648,11 +663,11 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
           const int rq = gq * p.R + j;   // row of the merge kernel's layout
           const size_t prow = ((size_t)pg * p.n_kv + (size_t)hk * S + split) * p.rows_pad + rq;
           __nv_bfloat16* orow = p.o + (size_t)(b * p.R + j) * qd + (size_t)(hk * p.G + gq) * 128;
-          const int h = 64 * hf;   // this half's 64 output columns in one batch of TMEM loads
-          float o64[64];
+          const int h = kODims * hf;   // this part's output columns in one batch of TMEM loads
+          float o64[kODims];
           if (have) {
-            tmem_ld32_issue(o_tm + (uint32_t)h, o64);
-            tmem_ld32_issue(o_tm + (uint32_t)(h + 32), o64 + 32);
+#pragma unroll
+            for (int c32 = 0; c32 < kODims; c32 += 32) tmem_ld32_issue(o_tm + (uint32_t)(h + c32), o64 + c32);
             tmem_wait_ld();
             // the buffer is read: the item after next may overwrite it
             tc_fence_before();
@@ -660,11 +675,11 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
             if (lane == 0) mbar_arrive(&o_free[ob]);
           } else {
 #pragma unroll
-            for (int i2 = 0; i2 < 64; ++i2) o64[i2] = 0.f;
+            for (int i2 = 0; i2 < kODims; ++i2) o64[i2] = 0.f;
           }
           if (rvalid) {
 #pragma unroll
-            for (int cc = 0; cc < 64; cc += 16) {
+            for (int cc = 0; cc < kODims; cc += 16) {
               const float* o16 = o64 + cc;
               const int c = h + cc;
               if (S == 1 && p.o_plane == kF16Plane) {   // one fp16 plane
@@ -717,14 +732,14 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
   }
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag && (warp == 8 || warp == 10) && lane == 0) {
+  if (*abort_flag && (warp == kWarpQK || warp == kWarpV) && lane == 0) {
     // let every load still in flight land before the shared memory goes away
     if (q_loads > 0) (void)mbar_wait(q_full, (uint32_t)((q_loads - 1) & 1), nullptr);
-    uint64_t* full = warp == 8 ? k_full : v_full;
+    uint64_t* full = warp == kWarpQK ? k_full : v_full;
     for (int t = max(0, issued - kUStages); t < issued; ++t)
       (void)mbar_wait(&full[t % kUStages], (uint32_t)((t / kUStages) & 1), nullptr);
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     if (lane == 0) (void)mbar_wait(mma_done, 0u, nullptr);   // MMAs done before TMEM is freed
     __syncwarp();
     tc_fence_after();
@@ -737,7 +752,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
 size_t attn_umma_smem_bytes() {
   return 1024 + 2 * kUQHalf + kUStages * kUStage + 4 * kUPPlane +
          (2 + 4 * kUStages + 8 + 1 + 4 + 2 * kUSlots + 1) * 8 + 16 + kUSlots * kUItem * sizeof(int) +
-         (2 * 2 * 128 + 2 * 2 * 128) * sizeof(float);
+         (2 * kParts * 128 + 2 * kParts * 128) * sizeof(float);
 }
 
 cudaError_t launch_attention_umma(const AttnUParams& p, int B, int grid, cudaStream_t s) {
