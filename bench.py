@@ -381,6 +381,10 @@ def main():
     ap.add_argument("--target-r", default="1,2,9,17,33,65,129,257,513,1025")
     ap.add_argument("--k-sweep", default="16,32,64,128",
                     help="block lengths of the context-4096 K sweep reported beside the headline ('' to skip)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (a smaller case, e.g. for a profiler capture)")
+    ap.add_argument("--ctx-max", type=int, default=None,
+                    help="cap the workload's context lengths (a smaller case, e.g. for a profiler capture)")
     ap.add_argument("--conditioning", default="kv", choices=["kv", "input", "none"],
                     help="how the target context conditions the draft: K/V injection (the method), "
                          "input fusion or none (the ablation variants)")
@@ -396,6 +400,11 @@ def main():
 
     from synth import CONFIGS
     s = CONFIGS[args.config]
+    if args.batch:
+        s = s.with_(batch=args.batch)
+    if args.ctx_max:
+        kind, *lim = s.ctx
+        s = s.with_(ctx=(kind, *[min(int(v), args.ctx_max) for v in lim]))
     K = args.K or s.K
     if K > s.K_max:
         s = s.with_(K_max=K)
