@@ -348,6 +348,7 @@ struct dflash_ctx {
   bool gemm_pairs = true;                // two token tiles of a split operand per CTA
   bool gemm_direct = true;               // single-split tiles: epilogue straight from tensor memory
   int gemm_bn_max = 192;                 // widest plain-operand token tile (MMA N)
+  bool gemm_persist = true;              // multi-wave one-split GEMMs on the persistent instance
   bool lm_fused = false;                 // LM head as one GEMM with the argmax in its epilogue (every M)
   // With fuse_append, an append of <= 128 rows leaves its per-layer K/V
   // projection pending: the next draft's QKV GEMMs take the rows u along (each
@@ -441,6 +442,9 @@ void trace_end(dflash_ctx* c, int i, cudaStream_t s) {
   if (i >= 0 && cudaEventRecordWithFlags(c->ev[2 * i + 1], s, cudaEventRecordExternal) != cudaSuccess)
     cudaGetLastError();
 }
+
+// tensor-memory columns of an accumulator of n columns (allocation granularity)
+uint32_t tmem_cols_for_host(int n) { return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : n <= 256 ? 256u : 512u; }
 
 // cached token tensor map: bf16 [planes][M][K], box BN x 64, 128-byte swizzle
 int get_xmap(dflash_ctx* c, const void* x, int K, int M, int BN, int planes, const CUtensorMap** out) {
@@ -577,6 +581,14 @@ GemmPlan plan_gemm(const dflash_ctx* c, int M, int K, const SegRef* segs, int ns
         g.stages = pst;
         g.resident = pres;
         g.n_tiles /= 2;
+        // more pairs than SMs with plain operands: the persistent instance, whose
+        // two accumulators of gate + up columns fit tensor memory at 128-row
+        // token tiles (2 x 2 x 128 columns)
+        if (c->gemm_persist && g.XP == 1 && g.BN > 128 && g.n_tiles * g.t_tiles > c->num_sms) {
+          g.t_tiles = (M + 127) / 128;
+          g.BN = ((M + g.t_tiles - 1) / g.t_tiles + 15) / 16 * 16;
+          g.t_groups = g.t_tiles;
+        }
       }
     }
   }
@@ -671,7 +683,27 @@ int run_gemm_tc(dflash_ctx* c, const void* x, int M, int K, const SegRef* segs, 
   const double out_bytes = op.epi == EPI_ARGMAX ? (op.logits ? 4.0 * M * N : 8.0 * M) : 4.0 * M * N;
   const int tr = op.trace ? trace_begin(c, DFLASH_TRACE_GEMM, 2.0 * ((double)N * K + (double)M * K) + out_bytes, s)
                          : -1;
-  CK(launch_gemm_tc(p, n_tiles, splits, t_tiles, stages, s));
+  // more one-split tiles than SMs: the persistent instance, one CTA per SM
+  // with two accumulators, so that each tile's epilogue runs under the next
+  // tile's mainloop (plain operands, one token tile per CTA)
+  const int wb = pl.wpair ? 2 : 1;
+  const bool persist = c->gemm_persist && pl.direct && XP == 1 && pl.tt == 1 && !fuse &&
+                       (op.epi == EPI_QKV || op.epi == EPI_CTXKV || op.epi == EPI_RESID || op.epi == EPI_Y_SS ||
+                        (op.epi == EPI_SILU && pl.wpair)) &&
+                       (int64_t)n_tiles * t_tiles > c->num_sms && 2 * tmem_cols_for_host(BN * wb) <= 512;
+  if (persist) {
+    const size_t fixed = gemm_tc_persist_smem_bytes(BN, 0, wb);
+    const size_t stage = (size_t)wb * kTileRows * kTileK * 2 + (size_t)BN * kTileK * 2;
+    p.stages = (int)std::min<size_t>(8, ((size_t)227 * 1024 - fixed) / (stage + 16));
+    p.p_tiles = n_tiles * t_tiles;
+    p.p_ttiles = t_tiles;
+  }
+  if (persist && p.stages >= 2) {
+    CK(launch_gemm_tc_persist(p, std::min(c->num_sms, p.p_tiles), s));
+  } else {
+    p.stages = stages;
+    CK(launch_gemm_tc(p, n_tiles, splits, t_tiles, stages, s));
+  }
   trace_end(c, tr, s);
   c->launches += 1;
   return DFLASH_OK;
@@ -1685,6 +1717,8 @@ static int create_impl(const dflash_config* cfg, const dflash_weights* w, int32_
     c->graph_drafts = !(gg && gg[0] == '0');
     const char* gd = getenv("DFLASH_GEMM_DIRECT");   // 0: single-split tiles also reduce through ws
     c->gemm_direct = !(gd && gd[0] == '0');
+    const char* gpe = getenv("DFLASH_GEMM_PERSIST");   // 0: multi-wave one-split GEMMs one tile per CTA
+    if (gpe && gpe[0] == '0') c->gemm_persist = false;
     const char* gb = getenv("DFLASH_GEMM_BN_MAX");   // widest plain token tile, 64..256 in steps of 16
     if (gb) c->gemm_bn_max = std::max(64, std::min(256, atoi(gb) / 16 * 16));
     const char* gc = getenv("DFLASH_GEMM_CTAS");

@@ -462,6 +462,239 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
   }
 }
 
+// Persistent direct GEMM for grids of more tiles than SMs (large M, plain fp16
+// token operands, one token tile per CTA and one split): one CTA per SM walks
+// the tiles blockIdx.x, blockIdx.x + gridDim.x, ... (token tiles of a weight
+// tile adjacent, so concurrent CTAs share its boxes in L2).  The producer runs
+// the stage ring on across tiles, the MMA issuer alternates between two TMEM
+// accumulators, and the eight epilogue warps finish tile j from one of them
+// while tile j + 1 accumulates in the other -- the epilogue, 40-50% of a
+// one-tile CTA's time at the serving batch, runs under the next mainloop.  The
+// epilogue scratch has its own shared memory (the ring is never idle here).
+__global__ void __launch_bounds__(320, 1) gemm_tc_persist_kernel(const __grid_constant__ TcGemmParams p) {
+  constexpr int EW = 8;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+
+  const int S = p.stages, BN = p.BN;
+  const uint32_t w_box = kTileRows * kTileK * 2;
+  const int W = p.wpair ? 2 : 1;
+  const uint32_t a_bytes = w_box * (uint32_t)W;
+  const uint32_t b_bytes = (uint32_t)BN * kTileK * 2;   // one fp16 token box
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + (size_t)S * a_bytes;
+  float* epi_sm = reinterpret_cast<float*>(sB + (size_t)S * b_bytes);   // [2 halves][kEpiChunk][kEpiLd]
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi_sm + 2 * kEpiChunk * kEpiLd);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;    // [2]
+  uint64_t* acc_empty = acc_full + 2;   // [2]
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* wait_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
+  float* row_sc = reinterpret_cast<float*>(tmem_slot + 4);
+  long long* tdst = reinterpret_cast<long long*>(row_sc + 256);
+  int* tpos = reinterpret_cast<int*>(tdst + kStageTok);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  const int T = p.p_tiles, TX = p.p_ttiles;   // tiles, token tiles per weight tile
+  const uint32_t ncols = tmem_cols_for(BN * W);   // one accumulator
+  auto decode = [&](int tau, int& tile, int& seg, int& row0, int& n0) {
+    tile = tau / TX;
+    n0 = (tau % TX) * BN;
+    seg = 0;
+    if (W == 2) {
+      row0 = tile * kTileRows;
+    } else {
+      while (seg + 1 < p.nseg && tile >= p.seg_tile0[seg + 1]) ++seg;
+      row0 = (tile - p.seg_tile0[seg]) * kTileRows;
+    }
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 1);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == EW + 1) {
+    tmem_alloc(tmem_slot, 2 * ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  bool ok = true;
+  int issued = 0;   // producer: k-blocks whose loads were issued (over all tiles)
+  if (warp == EW) {
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      int pre = 0;
+      if ((int)blockIdx.x < T) {   // the first tile's first weight boxes before the dependency
+        int tile, seg, row0, n0;
+        decode(blockIdx.x, tile, seg, row0, n0);
+        pre = min(S, p.nkb);
+        tma_prefetch_desc(&p.tm_w[seg]);
+        if (W == 2) tma_prefetch_desc(&p.tm_w[1]);
+        for (int kb = 0; kb < pre; ++kb) {
+          mbar_expect_tx(&full[kb], a_bytes);
+          for (int w = 0; w < W; ++w)
+            tma_load_2d_hint(sA + (size_t)kb * a_bytes + w * w_box, &p.tm_w[seg + w], kb * kTileK, row0, &full[kb],
+                             pol);
+        }
+      }
+      pdl_wait();
+      tma_prefetch_desc(&p.tm_x);
+      int g = 0;
+      for (int tau = blockIdx.x; tau < T && ok; tau += gridDim.x) {
+        int tile, seg, row0, n0;
+        decode(tau, tile, seg, row0, n0);
+        for (int kb = 0; kb < p.nkb; ++kb, ++g) {
+          const int st = g % S;
+          const int kc = kb * kTileK;
+          if (g >= pre) {
+            if (!mbar_wait(&empty[st], (uint32_t)((g / S) & 1) ^ 1u, abort_flag, p.flags)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[st], a_bytes + b_bytes);
+            for (int w = 0; w < W; ++w)
+              tma_load_2d_hint(sA + (size_t)st * a_bytes + w * w_box, &p.tm_w[seg + w], kc, row0, &full[st], pol);
+          } else {
+            mbar_arrive_expect_tx(&full[st], b_bytes);
+          }
+          tma_load_3d(sB + (size_t)st * b_bytes, &p.tm_x, kc, n0, 0, &full[st]);
+          issued = g + 1;
+        }
+      }
+    } else {
+      pdl_wait();
+    }
+  } else if (warp == EW + 1) {
+    pdl_wait();
+    if (lane == 0) {
+      const uint32_t idesc = p.op16 ? umma_idesc_f16(kTileRows, BN) : umma_idesc_bf16(kTileRows, BN);
+      int g = 0, j = 0;
+      for (int tau = blockIdx.x; tau < T && ok; tau += gridDim.x, ++j) {
+        const int a = j & 1;
+        // the epilogue of tile j - 2 has read this accumulator
+        if (!mbar_wait(&acc_empty[a], (uint32_t)((j >> 1) & 1) ^ 1u, abort_flag, p.flags)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < p.nkb; ++kb, ++g) {
+          const int st = g % S;
+          if (!mbar_wait(&full[st], (uint32_t)((g / S) & 1), abort_flag, p.flags)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + (size_t)st * b_bytes));
+          for (int w = 0; w < W; ++w) {
+            const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + (size_t)st * a_bytes + w * w_box));
+#pragma unroll
+            for (int k = 0; k < kTileK / 16; ++k)
+              umma_bf16(tmem + (uint32_t)a * ncols + (uint32_t)(w * BN), ad + 2u * k, bd + 2u * k, idesc,
+                        (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[st]);
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[a]);
+      }
+      umma_commit(mma_done);
+    }
+  } else {
+    // eight epilogue warps, two per tensor-memory lane quadrant, as in the
+    // one-tile direct instance; between tiles both halves meet, then the
+    // accumulator is handed back to the MMA issuer
+    pdl_wait();
+    const int half = warp >> 2;
+    const int r = threadIdx.x & 127;
+    int j = 0;
+    for (int tau = blockIdx.x; tau < T && ok; tau += gridDim.x, ++j) {
+      int tile, seg, row0, n0;
+      decode(tau, tile, seg, row0, n0);
+      const int a = j & 1;
+      const uint32_t par = (uint32_t)((j >> 1) & 1);
+      const int t_end = min(n0 + BN, p.M);
+      if (half == 0) {
+        if (n0 < t_end) {
+          if (p.epi == EPI_QKV || p.epi == EPI_CTXKV)
+            for (int c = n0; c < t_end; c += 128)
+              rope_kv_stage(p, r, seg, row0, c, min(128, t_end - c), p.epi == EPI_CTXKV, tpos + (c - n0),
+                            tdst + (c - n0));
+          if (p.epi == EPI_QKV || p.epi == EPI_CTXKV || p.epi == EPI_SILU) row_scales(p, r, n0, t_end - n0, row_sc);
+          epi_bar();
+        }
+        if (!group_wait(r, &acc_full[a], par, abort_flag, p.flags, wait_flag)) ok = false;
+      }
+      epi_pair_bar();   // staging done, accumulator verdict in *wait_flag
+      if (half == 1) {
+        ok = *wait_flag != 0;
+        if (ok) (void)mbar_wait(&acc_full[a], par, nullptr);
+      }
+      if (ok) {
+        tc_fence_after();
+        const int nch = (t_end - n0 + kEpiChunk - 1) / kEpiChunk;
+        const int mid = min(t_end, n0 + kEpiChunk * ((nch + 1) / 2));
+        const int lo = half ? mid : n0, hi = half ? t_end : mid;
+        float* sm = epi_sm + half * kEpiChunk * kEpiLd;
+        const TmemRed red{tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)a * ncols, n0, BN, 0, BN};
+        const int bar = 1 + half;
+        const int off = lo - n0;
+        if (lo < hi) {
+          switch (p.epi) {
+            case EPI_QKV:
+              epi_rope_kv(p, red, r, seg, row0, lo, hi, sm, row_sc + off, false, tpos + off, tdst + off, 2, bar);
+              break;
+            case EPI_CTXKV:
+              epi_rope_kv(p, red, r, seg, row0, lo, hi, sm, row_sc + off, true, tpos + off, tdst + off, 2, bar);
+              break;
+            case EPI_RESID: epi_resid(p, red, r, tile, seg, row0, lo, hi, sm, true, bar); break;
+            case EPI_Y_SS: epi_resid(p, red, r, tile, seg, row0, lo, hi, sm, false, bar); break;
+            case EPI_SILU: epi_silu(p, red, r, tile, lo, hi, row_sc + off); break;
+            default: break;
+          }
+        }
+      }
+      // both halves are done with this accumulator and the staged tables
+      tc_fence_before();
+      epi_pair_bar();
+      ok = ok && *wait_flag != 0;
+      if (threadIdx.x == 0) mbar_arrive(&acc_empty[a]);
+    }
+  }
+
+  if (!ok) {
+    *abort_flag = 1;
+    set_flag(p.flags, DFLASH_FLAG_WAIT_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && warp == EW && lane == 0) {
+    for (int g = max(0, issued - S); g < issued; ++g) (void)mbar_wait(&full[g % S], (uint32_t)((g / S) & 1), nullptr);
+  }
+  if (warp == EW + 1) {
+    if (lane == 0) (void)mbar_wait(mma_done, 0u, nullptr);   // every MMA done before TMEM is freed
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * ncols);
+  }
+}
+
 }  // namespace
 
 size_t gemm_tc_smem_bytes(int BN, int stages, int x_planes, int tt, int w_boxes) {
@@ -526,6 +759,25 @@ int gemm_tc_resident_ctas(int tt, bool direct, size_t smem, int n_cols) {
   const int by_threads = prop.maxThreadsPerMultiProcessor / threads;
   const int by_tmem = 512 / (int)tmem_cols_for(n_cols);
   return std::max(0, std::min({by_regs, by_smem, by_threads, by_tmem, prop.maxBlocksPerMultiProcessor}));
+}
+
+size_t gemm_tc_persist_smem_bytes(int BN, int stages, int w_boxes) {
+  const size_t per_stage = (size_t)w_boxes * kTileRows * kTileK * 2 + (size_t)BN * kTileK * 2;
+  return 1024 + (size_t)stages * per_stage + 2 * kEpiChunk * kEpiLd * sizeof(float) + (size_t)(2 * stages + 5) * 8 +
+         16 + 256 * sizeof(float) + kStageTok * (sizeof(long long) + sizeof(int));
+}
+
+cudaError_t launch_gemm_tc_persist(const TcGemmParams& p, int grid, cudaStream_t s) {
+  static size_t allowed = 0;
+  const size_t smem = gemm_tc_persist_smem_bytes(p.BN, p.stages, p.wpair ? 2 : 1);
+  if (smem > allowed) {
+    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
+    if (e != cudaSuccess) return e;
+    allowed = smem;
+  }
+  const cudaError_t e = launch_k(gemm_tc_persist_kernel, dim3(grid), dim3(320), smem, s, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_gemm_tc(const TcGemmParams& p, int n_tiles, int splits, int t_tiles, int stages,

@@ -163,6 +163,7 @@ struct TcGemmParams : EpiArgs {
                                 //    (no partials in ws, no counters)
   int wpair;                    // 1 (EPI_SILU, direct, tt = 1): CTA y computes gate tile y and up
                                 //    tile y (two weight boxes per stage, two accumulators)
+  int p_tiles, p_ttiles;        // persistent instance: tiles, token tiles per weight tile
 };
 
 
@@ -231,6 +232,8 @@ cudaError_t launch_attention_tc(const AttnTcParams& p, int n_consumer_warps, int
 void launch_argmax_finalize(unsigned long long* keys, int rows, int32_t* ids, cudaStream_t s);
 
 size_t gemm_tc_smem_bytes(int BN, int stages, int x_planes, int tt, int w_boxes = 1);
+size_t gemm_tc_persist_smem_bytes(int BN, int stages, int w_boxes);
+cudaError_t launch_gemm_tc_persist(const TcGemmParams& p, int grid, cudaStream_t s);
 int gemm_tc_resident_ctas(int tt, bool direct, size_t smem, int n_cols);
 cudaError_t launch_gemm_tc(const TcGemmParams& p, int n_tiles, int splits, int t_tiles, int stages,
                            cudaStream_t s);
