@@ -677,6 +677,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
 #pragma unroll
             for (int i2 = 0; i2 < kODims; ++i2) o64[i2] = 0.f;
           }
+          bool bad = false;   // an fp16 output out of range, latched once below
           if (rvalid) {
 #pragma unroll
             for (int cc = 0; cc < kODims; cc += 16) {
@@ -686,8 +687,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
                 uint32_t wh[8];
 #pragma unroll
                 for (int i2 = 0; i2 < 8; ++i2) {
-                  check_f16(o16[2 * i2] * inv, p.flags);
-                  check_f16(o16[2 * i2 + 1] * inv, p.flags);
+                  bad |= f16_out_of_range(o16[2 * i2] * inv) || f16_out_of_range(o16[2 * i2 + 1] * inv);
                   const __half2 v = __floats2half2_rn(o16[2 * i2] * inv, o16[2 * i2 + 1] * inv);
                   wh[i2] = *reinterpret_cast<const uint32_t*>(&v);
                 }
@@ -719,6 +719,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
               }
             }
           }
+          if (bad) set_flag(p.flags, DFLASH_FLAG_F16_RANGE);
           if (rvalid && S > 1 && hf == 0) p.part_lse[prow] = lse;
         }
       }

@@ -274,11 +274,25 @@ __device__ __forceinline__ void check_f16(float x, uint32_t* flags) {
   if (!(fabsf(x) <= 65504.0f)) set_flag(flags, DFLASH_FLAG_F16_RANGE);
 }
 
+// Whether x lies outside fp16's range (|x| > 65504, or NaN).
+__device__ __forceinline__ bool f16_out_of_range(float x) { return !(fabsf(x) <= 65504.0f); }
+
 // A token operand written as one fp16 plane instead (11 significant bits, one
 // MMA against fp16 copies of the weights): the lo-plane offset kF16Plane says so.
 __device__ __forceinline__ void put_op(float x, __nv_bfloat16* hi, size_t plane, uint32_t* flags) {
   if (plane == kF16Plane) {
     check_f16(x, flags);
+    *reinterpret_cast<__half*>(hi) = __float2half_rn(x);
+  } else {
+    split_bf16(x, hi, hi + plane);
+  }
+}
+// The same inside a loop: an fp16 value out of range only raises `bad`, which
+// the caller latches once after the loop (a flag write per value, even
+// predicated off, weighs on the unrolled epilogues' instruction stream).
+__device__ __forceinline__ void put_op_acc(float x, __nv_bfloat16* hi, size_t plane, bool& bad) {
+  if (plane == kF16Plane) {
+    bad |= f16_out_of_range(x);
     *reinterpret_cast<__half*>(hi) = __float2half_rn(x);
   } else {
     split_bf16(x, hi, hi + plane);

@@ -421,6 +421,7 @@ __device__ void epi_resid(const EpiArgs& p, const Red& red, int r, int tile, int
   if constexpr (Red::kTmem) {
     for (int c0 = n0; c0 < t_hi; c0 += kEpiChunk) {
       const int cn = min(kEpiChunk, t_hi - c0);
+      bool bad = false;      // an fp16 operand out of range in this chunk
       float hv[kEpiChunk];   // the chunk's residual rows, every load in flight at once
       if (add) {
 #pragma unroll
@@ -441,13 +442,14 @@ __device__ void epi_resid(const EpiArgs& p, const Red& red, int r, int tile, int
           if (i < n) {
             if (p.h != nullptr) p.h[(size_t)t * p.N + gcol] = v;
             if (p.xn_out != nullptr)
-              put_op(v * gain, p.xn_out + (size_t)t * p.N + gcol, p.op16 ? kF16Plane : (size_t)p.M * p.N, p.flags);
+              put_op_acc(v * gain, p.xn_out + (size_t)t * p.N + gcol, p.op16 ? kF16Plane : (size_t)p.M * p.N, bad);
           }
           sq[i] = v * v;   // slots past n are summed but never stored
         }
         const float ss = warp_sum8(sq, lane);
         if ((lane & 3) == 0 && slot < n) sm[warp * kEpiChunk + i0 + slot] = ss;
       }
+      if (bad) set_flag(p.flags, DFLASH_FLAG_F16_RANGE);
       epi_bar(bar);
       if (r < cn) {
         const float ss = sm[r] + sm[kEpiChunk + r] + sm[2 * kEpiChunk + r] + sm[3 * kEpiChunk + r];
@@ -458,6 +460,7 @@ __device__ void epi_resid(const EpiArgs& p, const Red& red, int r, int tile, int
   } else {
     for (int c0 = n0; c0 < t_hi; c0 += kEpiChunk) {
       const int cn = min(kEpiChunk, t_hi - c0);
+      bool bad = false;
       for (int i0 = 0; i0 < cn; i0 += kRedTok) {
         const int n = min(kRedTok, cn - i0);
         float acc[kRedTok], hv[kRedTok];
@@ -473,11 +476,12 @@ __device__ void epi_resid(const EpiArgs& p, const Red& red, int r, int tile, int
           const float v = add ? acc[i] + hv[i] : acc[i];
           if (p.h != nullptr) p.h[(size_t)t * p.N + gcol] = v;
           if (p.xn_out != nullptr)
-            put_op(v * gain, p.xn_out + (size_t)t * p.N + gcol, p.op16 ? kF16Plane : (size_t)p.M * p.N, p.flags);
+            put_op_acc(v * gain, p.xn_out + (size_t)t * p.N + gcol, p.op16 ? kF16Plane : (size_t)p.M * p.N, bad);
           const float sq = warp_sum(v * v);
           if (lane == 0) sm[warp * kEpiChunk + i0 + i] = sq;
         }
       }
+      if (bad) set_flag(p.flags, DFLASH_FLAG_F16_RANGE);
       epi_bar(bar);
       if (r < cn) {
         const float ss = sm[r] + sm[kEpiChunk + r] + sm[2 * kEpiChunk + r] + sm[3 * kEpiChunk + r];
@@ -600,6 +604,7 @@ template <class Red>
 __device__ void epi_silu(const EpiArgs& p, const Red& red, int r, int pair, int n0, int t_hi, const float* sc) {
   const int I = p.seg_rows[0];
   const int f = pair * kTileRows + r;
+  bool bad = false;   // an fp16 operand out of range, latched once at the end
   if constexpr (Red::kTmem) {   // gate and up sums of 16 tokens in one batch of loads
     for (int t0 = n0; t0 < t_hi; t0 += 16) {
       const int n = min(16, t_hi - t0);
@@ -610,10 +615,11 @@ __device__ void epi_silu(const EpiArgs& p, const Red& red, int r, int pair, int 
       for (int i = 0; i < 16; ++i) {
         if (i >= n) break;
         const float gs = g[i] * sc[t0 + i - n0], us = u[i] * sc[t0 + i - n0];
-        put_op(gs / (1.0f + expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
-               p.op16 ? kF16Plane : (size_t)p.M * I, p.flags);
+        put_op_acc(gs / (1.0f + expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
+                   p.op16 ? kF16Plane : (size_t)p.M * I, bad);
       }
     }
+    if (bad) set_flag(p.flags, DFLASH_FLAG_F16_RANGE);
     return;
   }
   for (int t0 = n0; t0 < t_hi; t0 += kRedTok) {
@@ -624,10 +630,11 @@ __device__ void epi_silu(const EpiArgs& p, const Red& red, int r, int pair, int 
     for (int i = 0; i < kRedTok; ++i) {
       if (i >= n) break;
       const float gs = g[i] * sc[t0 + i - n0], us = u[i] * sc[t0 + i - n0];
-      put_op(gs / (1.0f + expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
-             p.op16 ? kF16Plane : (size_t)p.M * I, p.flags);
+      put_op_acc(gs / (1.0f + expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
+                 p.op16 ? kF16Plane : (size_t)p.M * I, bad);
     }
   }
+  if (bad) set_flag(p.flags, DFLASH_FLAG_F16_RANGE);
 }
 
 }  // namespace
