@@ -111,6 +111,15 @@ __device__ __forceinline__ void rope_cs(int pos, uint64_t turns, float* c, float
   const float x = (float)(uint32_t)(ph >> 32) * 4.656612873077392578125e-10f;   // 2^-31
   sincospif(x, s, c);
 }
+// The same reduction, with the hardware sin / cos on pi * x for x taken into
+// [-1, 1) (absolute error ~1e-6, three orders below the bf16 rounding of the
+// rotated q and K rows it serves): the tensor-core epilogues rotate hundreds
+// of tokens per thread, where the library routine's code and latency dominate.
+__device__ __forceinline__ void rope_cs_fast(int pos, uint64_t turns, float* c, float* s) {
+  const uint64_t ph = (uint64_t)(uint32_t)pos * turns;
+  const int32_t q = (int32_t)(uint32_t)(ph >> 32);   // turns as a signed 0.32 fraction: [-1/2, 1/2)
+  __sincosf((float)q * 1.46291808e-9f, s, c);           // 2 pi / 2^32 rad per unit
+}
 
 // ---------------------------------------------------------------- timing / waits
 

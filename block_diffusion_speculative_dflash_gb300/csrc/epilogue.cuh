@@ -368,7 +368,7 @@ __device__ void epi_rope_kv(const EpiArgs& p, const Red& red, int r, int seg, in
           y[u] = sm[ii * kEpiLd + r];
           if (!is_v) {
             float c, s;
-            rope_cs(cpos[ii], f, &c, &s);
+            rope_cs_fast(cpos[ii], f, &c, &s);
             const float x1 = sm[ii * kEpiLd + pi], x2 = sm[ii * kEpiLd + pi + 64];
             y[u] = r < 64 ? x1 * c - x2 * s : x2 * c + x1 * s;
           }
@@ -389,7 +389,7 @@ __device__ void epi_rope_kv(const EpiArgs& p, const Red& red, int r, int seg, in
         float y = sm[i * kEpiLd + r];
         if (!is_v) {
           float c, s;
-          rope_cs(cpos[i], f, &c, &s);
+          rope_cs_fast(cpos[i], f, &c, &s);
           const float x1 = sm[i * kEpiLd + pi], x2 = sm[i * kEpiLd + pi + 64];
           y = r < 64 ? x1 * c - x2 * s : x2 * c + x1 * s;
         }
@@ -615,7 +615,7 @@ __device__ void epi_silu(const EpiArgs& p, const Red& red, int r, int pair, int 
       for (int i = 0; i < 16; ++i) {
         if (i >= n) break;
         const float gs = g[i] * sc[t0 + i - n0], us = u[i] * sc[t0 + i - n0];
-        put_op_acc(gs / (1.0f + expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
+        put_op_acc(gs / (1.0f + __expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
                    p.op16 ? kF16Plane : (size_t)p.M * I, bad);
       }
     }
@@ -630,7 +630,7 @@ __device__ void epi_silu(const EpiArgs& p, const Red& red, int r, int pair, int 
     for (int i = 0; i < kRedTok; ++i) {
       if (i >= n) break;
       const float gs = g[i] * sc[t0 + i - n0], us = u[i] * sc[t0 + i - n0];
-      put_op_acc(gs / (1.0f + expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
+      put_op_acc(gs / (1.0f + __expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
                  p.op16 ? kF16Plane : (size_t)p.M * I, bad);
     }
   }
