@@ -135,6 +135,14 @@ __device__ __forceinline__ bool quarter_bar_and(int q, bool v) {
   return all != 0;
 }
 
+// 2^x by the MUFU approximation (one instruction; results below 2^-126 flush to
+// zero, far under the bf16 planes of P whose largest entry is ~1)
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -561,11 +569,19 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
           // past the row's own position) are masked
           const int pos0 = p_begin + t * kUTile + kPCols * hf;
           const int p_row = p.causal ? min(p_end, row_lim + 1) : p_end;
+          if (pos0 + kPCols <= p_row) {   // the whole half in range (every tile but a split's last)
 #pragma unroll
-          for (int i2 = 0; i2 < kPCols; ++i2) {
-            const float v = pos0 + i2 < p_row ? s[i2] * p.scale_log2 : -INFINITY;
-            s[i2] = v;
-            hmax = fmaxf(hmax, v);
+            for (int i2 = 0; i2 < kPCols; ++i2) {
+              s[i2] *= p.scale_log2;
+              hmax = fmaxf(hmax, s[i2]);
+            }
+          } else {
+#pragma unroll
+            for (int i2 = 0; i2 < kPCols; ++i2) {
+              const float v = pos0 + i2 < p_row ? s[i2] * p.scale_log2 : -INFINITY;
+              s[i2] = v;
+              hmax = fmaxf(hmax, v);
+            }
           }
         } else {
           ok = false;
@@ -620,7 +636,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
         float ps = 0.f;
 #pragma unroll
         for (int i2 = 0; i2 < kPCols / 2; ++i2) {
-          const float p0 = exp2f(s[2 * i2] - mr), p1 = exp2f(s[2 * i2 + 1] - mr);
+          const float p0 = ex2_ftz(s[2 * i2] - mr), p1 = ex2_ftz(s[2 * i2 + 1] - mr);
           ps += p0 + p1;
           // hi = p with its low 16 bits cleared (p >= 0: truncation, exact as
           // bf16), lo = the exact remainder rounded to bf16
