@@ -565,20 +565,18 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&s_free[sb]);
-          // scale into the log2 domain; positions past the split (and, causal,
-          // past the row's own position) are masked
+          // positions past the split (and, causal, past the row's own
+          // position) are masked; the scores stay unscaled (the log2-domain
+          // scale goes into the exponent's FMA below and into the maximum)
           const int pos0 = p_begin + t * kUTile + kPCols * hf;
           const int p_row = p.causal ? min(p_end, row_lim + 1) : p_end;
           if (pos0 + kPCols <= p_row) {   // the whole half in range (every tile but a split's last)
 #pragma unroll
-            for (int i2 = 0; i2 < kPCols; ++i2) {
-              s[i2] *= p.scale_log2;
-              hmax = fmaxf(hmax, s[i2]);
-            }
+            for (int i2 = 0; i2 < kPCols; ++i2) hmax = fmaxf(hmax, s[i2]);
           } else {
 #pragma unroll
             for (int i2 = 0; i2 < kPCols; ++i2) {
-              const float v = pos0 + i2 < p_row ? s[i2] * p.scale_log2 : -INFINITY;
+              const float v = pos0 + i2 < p_row ? s[i2] : -INFINITY;
               s[i2] = v;
               hmax = fmaxf(hmax, v);
             }
@@ -596,6 +594,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
         float tmax = xmax[(sb * kParts) * 128 + r];
 #pragma unroll
         for (int q2 = 1; q2 < kParts; ++q2) tmax = fmaxf(tmax, xmax[(sb * kParts + q2) * 128 + r]);
+        tmax *= p.scale_log2;   // the tile's row maximum in the log2 domain
         // reference maximum: set by the first tile (which always holds the
         // split's first position), raised only when a row outgrows it by more
         // than kRescale -- then O and l of that row are rescaled (both halves
@@ -628,7 +627,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
           tmem_wait_st();
           l *= factor;
         }
-        // P = 2^(s - m_ref) <= 2^kRescale as split bf16
+        // P = 2^(s * scale - m_ref) <= 2^kRescale as split bf16
         // (a causal row may see no position of this split: its scores are all
         // -inf, and so is m_ref; 0 as the reference makes P = 0, l = 0)
         const float mr = m_ref == -INFINITY ? 0.f : m_ref;
@@ -636,7 +635,8 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
         float ps = 0.f;
 #pragma unroll
         for (int i2 = 0; i2 < kPCols / 2; ++i2) {
-          const float p0 = ex2_ftz(s[2 * i2] - mr), p1 = ex2_ftz(s[2 * i2 + 1] - mr);
+          const float p0 = ex2_ftz(fmaf(s[2 * i2], p.scale_log2, -mr)),
+                      p1 = ex2_ftz(fmaf(s[2 * i2 + 1], p.scale_log2, -mr));
           ps += p0 + p1;
           // hi = p with its low 16 bits cleared (p >= 0: truncation, exact as
           // bf16), lo = the exact remainder rounded to bf16
