@@ -31,9 +31,9 @@
 //            the row maximum of the tile from both halves (exchanged in shared
 //            memory), log2-domain softmax against a reference maximum that is
 //            only raised when a row's maximum grows by more than kRescale (then
-//            the row of O is rescaled in TMEM), P as split bf16 (hi + lo planes,
-//            two MMAs, ~16 significant bits) into shared memory, and at the end
-//            O / l out -- the final output (one split) or the split's normalised
+//            the row of O is rescaled in TMEM), P rounded to bf16 (the type of
+//            the V operand it meets) into shared memory, and at the end O / l
+//            out -- the final output (one split) or the split's normalised
 //            partial and log2-sum-exp for the merge kernel.
 // Softmax, the score buffers and the P buffers are double-buffered, so the
 // scores of tile t+1 are computed while the softmax of tile t runs.
@@ -163,6 +163,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 constexpr int kSoftWarps = 4 * kParts;
+// bf16 planes of P: 1 (round to nearest: 8 significant bits, like the bf16 V
+// it multiplies) or 2 (hi + lo, ~16 bits, two PV MMAs)
+constexpr int kPPlanes = 1;
 constexpr int kWarpQK = kSoftWarps, kWarpMma = kSoftWarps + 1, kWarpV = kSoftWarps + 2;
 constexpr int kUThreads = 32 * (kSoftWarps + 3);   // softmax warps, the query/K producer, the MMA issuer, the V producer
 constexpr int kUSlots = 4;       // work items published ahead of the consumers
@@ -236,8 +239,8 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* sQ = smem;                                   // 2 x [128 rows][64 dims]
   uint8_t* ring = sQ + 2 * kUQHalf;                     // kUStages x (K lo, K hi, V lo, V hi)
-  uint8_t* sP = ring + kUStages * kUStage;              // [2 buffers][hi, lo][128 rows][64 positions]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 4 * kUPPlane);
+  uint8_t* sP = ring + kUStages * kUStage;              // [2 buffers][kPPlanes][128 rows][64 positions]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kPPlanes * kUPPlane);
   uint64_t* q_full = bars;
   uint64_t* q_free = bars + 1;       // the item's last S MMA is done: the next queries may land
   // K and V of a stage have barriers of their own: a K slot is free once S has
@@ -443,8 +446,8 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
         const uint32_t vb = smem_u32(ring + (size_t)x.st * kUStage + 2 * kUBox);
         const uint32_t od = tmem + 128u + 128u * (uint32_t)x.ob;
 #pragma unroll
-        for (int pl = 0; pl < 2; ++pl) {
-          const uint64_t pa = sw128_kmajor_desc(smem_u32(sP + (size_t)(pb * 2 + pl) * kUPPlane));
+        for (int pl = 0; pl < kPPlanes; ++pl) {
+          const uint64_t pa = sw128_kmajor_desc(smem_u32(sP + (size_t)(pb * kPPlanes + pl) * kUPPlane));
 #pragma unroll
           for (int k = 0; k < kUTile / 16; ++k)   // 16 positions = two 8-row groups = 2048 B of V
             umma_bf16(od, pa + 2u * k, sw128_mnmajor_desc(vb + 2048u * k, kUBox, 1024u), idesc_o,
@@ -640,9 +643,13 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
           ps += p0 + p1;
           // hi = p with its low 16 bits cleared (p >= 0: truncation, exact as
           // bf16), lo = the exact remainder rounded to bf16
-          const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-          hi[i2] = __byte_perm(u0, u1, 0x7632);
-          lo[i2] = pack_bf16x2(p0 - __uint_as_float(u0 & 0xffff0000u), p1 - __uint_as_float(u1 & 0xffff0000u));
+          if constexpr (kPPlanes == 2) {
+            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+            hi[i2] = __byte_perm(u0, u1, 0x7632);
+            lo[i2] = pack_bf16x2(p0 - __uint_as_float(u0 & 0xffff0000u), p1 - __uint_as_float(u1 & 0xffff0000u));
+          } else {
+            hi[i2] = pack_bf16x2(p0, p1);
+          }
         }
         l += ps;
         const int pb = g & 1;
@@ -650,8 +657,8 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
           ok = false;
           continue;
         }
-        st_swizzled_part(sP + (size_t)(pb * 2) * kUPPlane, r, (kPCols / 8) * hf, hi);
-        st_swizzled_part(sP + (size_t)(pb * 2 + 1) * kUPPlane, r, (kPCols / 8) * hf, lo);
+        st_swizzled_part(sP + (size_t)(pb * kPPlanes) * kUPPlane, r, (kPCols / 8) * hf, hi);
+        if constexpr (kPPlanes == 2) st_swizzled_part(sP + (size_t)(pb * 2 + 1) * kUPPlane, r, (kPCols / 8) * hf, lo);
         fence_proxy_async_smem();   // generic-proxy P writes -> the tensor core's reads
         tc_fence_before();
         __syncwarp();
@@ -767,7 +774,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
 }  // namespace
 
 size_t attn_umma_smem_bytes() {
-  return 1024 + 2 * kUQHalf + kUStages * kUStage + 4 * kUPPlane +
+  return 1024 + 2 * kUQHalf + kUStages * kUStage + 2 * kPPlanes * kUPPlane +
          (2 + 4 * kUStages + 8 + 1 + 4 + 2 * kUSlots + 1) * 8 + 16 + kUSlots * kUItem * sizeof(int) +
          (2 * kParts * 128 + 2 * kParts * 128) * sizeof(float);
 }
