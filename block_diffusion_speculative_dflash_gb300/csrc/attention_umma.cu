@@ -630,17 +630,19 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
           tmem_wait_st();
           l *= factor;
         }
-        // P = 2^(s * scale - m_ref) <= 2^kRescale as split bf16
+        // P = 2^(s * scale - m_ref) <= 2^kRescale in bf16
         // (a causal row may see no position of this split: its scores are all
-        // -inf, and so is m_ref; 0 as the reference makes P = 0, l = 0)
+        // -inf, and so is m_ref; 0 as the reference makes P = 0, l = 0); the
+        // exponent's FMA and the row sum on pairs (packed fp32 instructions)
         const float mr = m_ref == -INFINITY ? 0.f : m_ref;
         uint32_t hi[kPCols / 2], lo[kPCols / 2];
-        float ps = 0.f;
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-mr, -mr);
+        float2 ps2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i2 = 0; i2 < kPCols / 2; ++i2) {
-          const float p0 = ex2_ftz(fmaf(s[2 * i2], p.scale_log2, -mr)),
-                      p1 = ex2_ftz(fmaf(s[2 * i2 + 1], p.scale_log2, -mr));
-          ps += p0 + p1;
+          const float2 x2 = __ffma2_rn(make_float2(s[2 * i2], s[2 * i2 + 1]), sc2, nm2);
+          const float p0 = ex2_ftz(x2.x), p1 = ex2_ftz(x2.y);
+          ps2 = __fadd2_rn(ps2, make_float2(p0, p1));
           // hi = p with its low 16 bits cleared (p >= 0: truncation, exact as
           // bf16), lo = the exact remainder rounded to bf16
           if constexpr (kPPlanes == 2) {
@@ -651,7 +653,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
             hi[i2] = pack_bf16x2(p0, p1);
           }
         }
-        l += ps;
+        l += ps2.x + ps2.y;
         const int pb = g & 1;
         if (!warp_wait(&p_free[pb], (uint32_t)((g >> 1) & 1) ^ 1u, abort_flag, p.flags)) {
           ok = false;
