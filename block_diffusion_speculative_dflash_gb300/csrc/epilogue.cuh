@@ -615,7 +615,7 @@ __device__ void epi_silu(const EpiArgs& p, const Red& red, int r, int pair, int 
       for (int i = 0; i < 16; ++i) {
         if (i >= n) break;
         const float gs = g[i] * sc[t0 + i - n0], us = u[i] * sc[t0 + i - n0];
-        put_op_acc(gs / (1.0f + __expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
+        put_op_acc(__fdividef(gs, 1.0f + __expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
                    p.op16 ? kF16Plane : (size_t)p.M * I, bad);
       }
     }
@@ -630,7 +630,7 @@ __device__ void epi_silu(const EpiArgs& p, const Red& red, int r, int pair, int 
     for (int i = 0; i < kRedTok; ++i) {
       if (i >= n) break;
       const float gs = g[i] * sc[t0 + i - n0], us = u[i] * sc[t0 + i - n0];
-      put_op_acc(gs / (1.0f + __expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
+      put_op_acc(__fdividef(gs, 1.0f + __expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
                  p.op16 ? kF16Plane : (size_t)p.M * I, bad);
     }
   }
