@@ -356,9 +356,9 @@ int dflash_target_commit(dflash_target* t, const int32_t* keep, void* stream);
 int dflash_target_query(dflash_target* t, void* stream, int32_t* len, uint32_t* device_flags);
 
 /* ---------------------------------------------------------------- failure detection
- * (the survey's auxiliary subsystem: bounded device waits, allocation failures,
- * KV arena guard bands).  The pages have no counterpart for these: they are
- * the library's own error-handling surface.
+ * (bounded device waits, allocation failures, KV arena guard bands).  The
+ * method's description has no counterpart for these: they are the library's
+ * own error-handling surface.
  *
  * Time limit of every bounded wait in this context's kernels (mbarrier and
  * cross-CTA counter waits), in nanoseconds; 0 restores the default of 2 s.  A
