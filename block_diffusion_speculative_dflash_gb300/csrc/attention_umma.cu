@@ -51,7 +51,7 @@ constexpr uint32_t kUStage = 4 * kUBox;               // K[0:64], K[64:128], V[0
 constexpr uint32_t kUQHalf = 128 * 128;               // [128 rows][64 dims] bf16
 constexpr uint32_t kUPPlane = 128 * 128;              // [128 rows][64 positions] bf16
 constexpr float kRescale = 8.0f;                      // log2 headroom of P before O is rescaled
-constexpr uint32_t kUTmemCols = 512;                  // S[2] (2 x 64) + O[2] (2 x 128); grid mode: one O
+constexpr uint32_t kUTmemCols = 512;                  // S[2] (2 x 64) + one O (128) per softmax part
 
 // 32 lanes x 32 bits, 16 consecutive columns written from the thread's row.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
     fence_mbar_init();
   }
   constexpr bool grid_mode = !PERSIST;
-  const uint32_t tmem_cols = grid_mode ? kUTmemCols / 2 : kUTmemCols;
+  const uint32_t tmem_cols = kUTmemCols;
   if (warp == kWarpMma) {
     tmem_alloc(tmem_slot, tmem_cols);
     tmem_relinquish();
@@ -431,32 +431,34 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
         int g, st, ob, mi;
         bool first, last;
       };
-      // O[ob] += P(g) V(g): P hi and lo planes (K-major, 64 positions), V
-      // MN-major (rows = positions, 128 B of dims; the two 64-dim halves 8 KB
-      // apart); the first PV of an item overwrites the buffer, once the softmax
-      // has read the item that used it before
+      // O_h += P(g)[:, part h's positions] V(g)[those positions, :] for each
+      // softmax part h (its own reference maximum, so its own accumulator):
+      // P K-major (64 positions, 128-byte rows), V MN-major (rows = positions,
+      // 128 B of dims; the two 64-dim halves 8 KB apart); the first PV of an
+      // item overwrites the accumulators, once the softmax has read the last
+      // item's
       auto pv = [&](const Pv& x) -> bool {
         const int pb = x.g & 1;
         if (!mbar_wait(&p_full[pb], (uint32_t)((x.g >> 1) & 1), abort_flag, p.flags) ||
             !mbar_wait(&v_full[x.st], (uint32_t)((x.g / kUStages) & 1), abort_flag, p.flags))
           return false;
-        if (x.first && !mbar_wait(&o_free[x.ob], (uint32_t)((x.mi >> 1) & 1) ^ 1u, abort_flag, p.flags))
-          return false;
+        if (x.first && !mbar_wait(o_free, (uint32_t)(x.mi & 1) ^ 1u, abort_flag, p.flags)) return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(ring + (size_t)x.st * kUStage + 2 * kUBox);
-        const uint32_t od = tmem + 128u + 128u * (uint32_t)x.ob;
+        constexpr int kPerPart = kUTile / 16 / kParts;   // K = 16 steps of a part's positions
 #pragma unroll
         for (int pl = 0; pl < kPPlanes; ++pl) {
           const uint64_t pa = sw128_kmajor_desc(smem_u32(sP + (size_t)(pb * kPPlanes + pl) * kUPPlane));
 #pragma unroll
           for (int k = 0; k < kUTile / 16; ++k)   // 16 positions = two 8-row groups = 2048 B of V
-            umma_bf16(od, pa + 2u * k, sw128_mnmajor_desc(vb + 2048u * k, kUBox, 1024u), idesc_o,
-                      (!x.first || pl != 0 || k != 0) ? 1u : 0u);
+            umma_bf16(tmem + 128u + 128u * (uint32_t)(k / kPerPart), pa + 2u * k,
+                      sw128_mnmajor_desc(vb + 2048u * k, kUBox, 1024u), idesc_o,
+                      (!x.first || pl != 0 || k % kPerPart != 0) ? 1u : 0u);
         }
         umma_commit(&v_empty[x.st]);
         umma_commit(&p_free[pb]);
         umma_commit(o_done);
-        if (x.last) umma_commit(&o_final[x.ob]);
+        if (x.last) umma_commit(o_final);
         return true;
       };
       int g = 0, mi = 0;   // K/V tiles and items with tiles so far
@@ -507,7 +509,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
             ok = false;
             break;
           }
-          prev = Pv{g, st, mi & 1, mi, t == 0, t == nt - 1};
+          prev = Pv{g, st, 0, mi, t == 0, t == nt - 1};
         }
         // the item's last PV at once, so that its output does not wait for
         // the next item's first tile
@@ -546,14 +548,13 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
       const int b = x.b, split = x.split, hk = x.hk, qt = x.qt, p_begin = x.p_begin, p_end = x.p_end, S = x.S,
                 pg = x.pg;
       const int nt = p_end > p_begin ? (p_end - p_begin + kUTile - 1) / kUTile : 0;
-      const int ob = mi & 1;
       const int gq = r % p.G, j = qt * p.JT + r / p.G;   // query head hk * G + gq, block row j
       const bool rvalid = j < p.R;
       const int row_lim = block_base(p.st, b) + j;       // causal: the row's own position
-      const uint32_t o_tm = tmem + lane_base + 128u + 128u * (uint32_t)ob;
-      float m_ref = -INFINITY, l = 0.f;                  // l: this half's share of the row sum
-      // a failed wait skips the rest of its tile; the pair leaves the loop
-      // together at the next meeting
+      const uint32_t o_tm = tmem + lane_base + 128u + 128u * (uint32_t)hf;   // this part's accumulator
+      // this part's reference maximum and row sum over its positions of every
+      // tile; the parts combine once, at the output
+      float m_ref = -INFINITY, l = 0.f;
       for (int t = 0; t < nt; ++t, ++g) {
         const int sb = g & 1;
         float s[kPCols];
@@ -586,25 +587,16 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
           }
         } else {
           ok = false;
-        }
-        // the row's maximum over the whole tile: this half's and the partner's
-        // (double-buffered by tile parity, so one meeting per tile suffices)
-        xmax[(sb * kParts + hf) * 128 + r] = hmax;
-        if (!quarter_bar_and(qq, ok)) {
-          ok = false;
           break;
         }
-        float tmax = xmax[(sb * kParts) * 128 + r];
-#pragma unroll
-        for (int q2 = 1; q2 < kParts; ++q2) tmax = fmaxf(tmax, xmax[(sb * kParts + q2) * 128 + r]);
-        tmax *= p.scale_log2;   // the tile's row maximum in the log2 domain
-        // reference maximum: set by the first tile (which always holds the
-        // split's first position), raised only when a row outgrows it by more
-        // than kRescale -- then O and l of that row are rescaled (both halves
-        // take the same decision from the same maximum)
+        const float tmax = hmax * p.scale_log2;   // this part's tile maximum in the log2 domain
+        // reference maximum: set by the part's first tile with a position in
+        // range (O and l are still 0 until then), raised only when the part's
+        // maximum grows by more than kRescale -- then the part's O and l are
+        // rescaled
         float factor = 1.f;
         bool resc = false;
-        if (t == 0) {
+        if (m_ref == -INFINITY) {
           m_ref = tmax;
         } else if (tmax > m_ref + kRescale) {
           factor = exp2f(m_ref - tmax);
@@ -616,11 +608,11 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
           // o_done is in phase g-1 or g: the parity wait is unambiguous
           if (!warp_wait(o_done, (uint32_t)((g - 1) & 1), abort_flag, p.flags)) {
             ok = false;
-            continue;
+            break;
           }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = kODims * hf; c < kODims * hf + kODims; c += 16) {
+          for (int c = 0; c < 128; c += 16) {
             float o16[16];
             tmem_ld16(o_tm + (uint32_t)c, o16);
 #pragma unroll
@@ -657,7 +649,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
         const int pb = g & 1;
         if (!warp_wait(&p_free[pb], (uint32_t)((g >> 1) & 1) ^ 1u, abort_flag, p.flags)) {
           ok = false;
-          continue;
+          break;
         }
         st_swizzled_part(sP + (size_t)(pb * kPPlanes) * kUPPlane, r, (kPCols / 8) * hf, hi);
         if constexpr (kPPlanes == 2) st_swizzled_part(sP + (size_t)(pb * 2 + 1) * kUPPlane, r, (kPCols / 8) * hf, lo);
@@ -667,40 +659,60 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
         if (lane == 0) mbar_arrive(&p_full[pb]);
       }
       // ------------------------------------------------ output: O / l
-      // the row sum from both halves, in half order (both threads get the same
-      // value); every softmax thread meets its partner here on every path
+      // the parts combine: their reference maxima and row sums meet in shared
+      // memory (every softmax thread meets its partners here on every path),
+      // each part's O is weighted by 2^(m_part - M), M the largest, and the
+      // sums are taken in part order (every thread of the row gets the same)
+      float* xm = xmax + (i & 1) * kParts * 128;
       float* xs = xsum + (i & 1) * kParts * 128;
+      xm[hf * 128 + r] = m_ref;
       xs[hf * 128 + r] = l;
       quarter_bar(qq);
-      float lrow = xs[r];
+      float w[kParts];
+      float mrow = xm[r];
 #pragma unroll
-      for (int q2 = 1; q2 < kParts; ++q2) lrow += xs[q2 * 128 + r];
+      for (int q2 = 1; q2 < kParts; ++q2) mrow = fmaxf(mrow, xm[q2 * 128 + r]);
+      float lrow = 0.f;
+#pragma unroll
+      for (int q2 = 0; q2 < kParts; ++q2) {
+        const float mq = xm[q2 * 128 + r];
+        w[q2] = mq == -INFINITY ? 0.f : exp2f(mq - mrow);
+        lrow += xs[q2 * 128 + r] * w[q2];
+      }
       if (ok) {
         const int qd = p.n_q * 128;
         const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
-        const float lse = lrow > 0.f ? m_ref + log2f(lrow) : -INFINITY;
+        const float lse = lrow > 0.f ? mrow + log2f(lrow) : -INFINITY;
         // the item's last PV has its own barrier: by now o_done may be anywhere
         // between the last two phases, so a parity wait on it would be ambiguous
-        const bool have = nt > 0 && warp_wait(&o_final[ob], (uint32_t)((mi >> 1) & 1), abort_flag, p.flags);
+        const bool have = nt > 0 && warp_wait(o_final, (uint32_t)(mi & 1), abort_flag, p.flags);
         if (nt > 0 && !have) ok = false;
         if (ok) {
           tc_fence_after();
           const int rq = gq * p.R + j;   // row of the merge kernel's layout
           const size_t prow = ((size_t)pg * p.n_kv + (size_t)hk * S + split) * p.rows_pad + rq;
           __nv_bfloat16* orow = p.o + (size_t)(b * p.R + j) * qd + (size_t)(hk * p.G + gq) * 128;
-          const int h = kODims * hf;   // this part's output columns in one batch of TMEM loads
+          const int h = kODims * hf;   // this thread's output columns, from every part's accumulator
           float o64[kODims];
+#pragma unroll
+          for (int i2 = 0; i2 < kODims; ++i2) o64[i2] = 0.f;
           if (have) {
 #pragma unroll
-            for (int c32 = 0; c32 < kODims; c32 += 32) tmem_ld32_issue(o_tm + (uint32_t)(h + c32), o64 + c32);
-            tmem_wait_ld();
-            // the buffer is read: the item after next may overwrite it
+            for (int q2 = 0; q2 < kParts; ++q2) {
+              const uint32_t oq = tmem + lane_base + 128u + 128u * (uint32_t)q2;
+#pragma unroll
+              for (int c32 = 0; c32 < kODims; c32 += 32) {
+                float v32[32];
+                tmem_ld32_issue(oq + (uint32_t)(h + c32), v32);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i2 = 0; i2 < 32; ++i2) o64[c32 + i2] = fmaf(v32[i2], w[q2], o64[c32 + i2]);
+              }
+            }
+            // the accumulators are read: the next item may overwrite them
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&o_free[ob]);
-          } else {
-#pragma unroll
-            for (int i2 = 0; i2 < kODims; ++i2) o64[i2] = 0.f;
+            if (lane == 0) mbar_arrive(o_free);
           }
           bool bad = false;   // an fp16 output out of range, latched once below
           if (rvalid) {
