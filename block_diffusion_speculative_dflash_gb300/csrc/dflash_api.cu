@@ -349,6 +349,7 @@ struct dflash_ctx {
   bool gemm_direct = true;               // single-split tiles: epilogue straight from tensor memory
   int gemm_bn_max = 192;                 // widest plain-operand token tile (MMA N)
   bool gemm_persist = true;              // multi-wave one-split GEMMs on the persistent instance
+  bool gemm_by_epi = true;               // split-K one-tile GEMMs on their epilogue's own instance
   bool lm_fused = false;                 // LM head as one GEMM with the argmax in its epilogue (every M)
   // With fuse_append, an append of <= 128 rows leaves its per-layer K/V
   // projection pending: the next draft's QKV GEMMs take the rows u along (each
@@ -544,7 +545,8 @@ GemmPlan plan_gemm(const dflash_ctx* c, int M, int K, const SegRef* segs, int ns
   g.stages = std::max(2, std::min(8, budget / stage_bytes));
   // the split CTAs of a tile wait for each other in the epilogue, so a split
   // grid must be resident at once: size it by the occupancy actually reached
-  const int resident = gemm_tc_resident_ctas(g.tt, false, gemm_tc_smem_bytes(g.BN, g.stages, g.XP, g.tt), n_cols);
+  const int resident = gemm_tc_resident_ctas(g.tt, false, gemm_tc_smem_bytes(g.BN, g.stages, g.XP, g.tt), n_cols,
+                                             c->gemm_by_epi ? op.epi : -1);
   g.resident = resident;
   ctas_per_sm = std::max(1, std::min(ctas_per_sm, resident));
   const int base = g.n_tiles * g.t_groups;
@@ -698,7 +700,7 @@ int run_gemm_tc(dflash_ctx* c, const void* x, int M, int K, const SegRef* segs, 
     CK(launch_gemm_tc_persist(p, std::min(c->num_sms, p.p_tiles), s));
   } else {
     p.stages = stages;
-    CK(launch_gemm_tc(p, n_tiles, splits, t_tiles, stages, s));
+    CK(launch_gemm_tc(p, n_tiles, splits, t_tiles, stages, s, c->gemm_by_epi));
   }
   trace_end(c, tr, s);
   c->launches += 1;
@@ -1715,6 +1717,8 @@ static int create_impl(const dflash_config* cfg, const dflash_weights* w, int32_
     c->gemm_direct = !(gd && gd[0] == '0');
     const char* gpe = getenv("DFLASH_GEMM_PERSIST");   // 0: multi-wave one-split GEMMs one tile per CTA
     if (gpe && gpe[0] == '0') c->gemm_persist = false;
+    const char* gei = getenv("DFLASH_GEMM_BY_EPI");   // 0: one split-K instance reads the epilogue at run time
+    if (gei && gei[0] == '0') c->gemm_by_epi = false;
     const char* gb = getenv("DFLASH_GEMM_BN_MAX");   // widest plain token tile, 64..256 in steps of 16
     if (gb) c->gemm_bn_max = std::max(64, std::min(256, atoi(gb) / 16 * 16));
     const char* gc = getenv("DFLASH_GEMM_CTAS");

@@ -619,19 +619,18 @@ __device__ void epi_silu(const EpiArgs& p, const Red& red, int r, int pair, int 
                    p.op16 ? kF16Plane : (size_t)p.M * I, bad);
       }
     }
-    if (bad) set_flag(p.flags, DFLASH_FLAG_F16_RANGE);
-    return;
-  }
-  for (int t0 = n0; t0 < t_hi; t0 += kRedTok) {
-    const int n = min(kRedTok, t_hi - t0);
-    float g[kRedTok], u[kRedTok];
-    red.pair(t0, n, g, u);
+  } else {
+    for (int t0 = n0; t0 < t_hi; t0 += kRedTok) {
+      const int n = min(kRedTok, t_hi - t0);
+      float g[kRedTok], u[kRedTok];
+      red.pair(t0, n, g, u);
 #pragma unroll
-    for (int i = 0; i < kRedTok; ++i) {
-      if (i >= n) break;
-      const float gs = g[i] * sc[t0 + i - n0], us = u[i] * sc[t0 + i - n0];
-      put_op_acc(__fdividef(gs, 1.0f + __expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
-                 p.op16 ? kF16Plane : (size_t)p.M * I, bad);
+      for (int i = 0; i < kRedTok; ++i) {
+        if (i >= n) break;
+        const float gs = g[i] * sc[t0 + i - n0], us = u[i] * sc[t0 + i - n0];
+        put_op_acc(__fdividef(gs, 1.0f + __expf(-gs)) * us, p.a_out + (size_t)(t0 + i) * I + f,
+                   p.op16 ? kF16Plane : (size_t)p.M * I, bad);
+      }
     }
   }
   if (bad) set_flag(p.flags, DFLASH_FLAG_F16_RANGE);

@@ -48,11 +48,15 @@ __host__ __device__ __forceinline__ uint32_t tmem_cols_for(int BN) {
 // TT token tiles of BN per CTA (1, or 2 for wide split operands); the one-tile
 // instance is the common drafting case and fits two CTAs per SM.  DIRECT: the
 // tiles have one split and the epilogue reads the accumulator in place (its own
-// instances, so that the split-K instances carry none of that code).
-template <int TT, bool DIRECT>
+// instances, so that the split-K instances carry none of that code).  E: the
+// epilogue (a GemmEpi) compiled in, or -1 for the one in the parameters; the
+// split-K one-tile instance, on every drafting step's critical path, has one
+// instance per epilogue so that each carries only its own code.
+template <int TT, bool DIRECT, int E>
 __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1)
     gemm_tc_kernel(const __grid_constant__ TcGemmParams p) {
   constexpr int EW = DIRECT ? 8 : 4;   // epilogue warps; warp EW: TMA producer, EW + 1: MMA issuer
+  const int epi = E >= 0 ? E : p.epi;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -211,11 +215,11 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
       // while the weights stream: the folded-norm row scales and every token's
       // RoPE position and destination (<= kStageTok tokens, 128 per pass)
       if (n0 < t_end) {
-        if (p.epi == EPI_QKV || p.epi == EPI_CTXKV)
+        if (epi == EPI_QKV || epi == EPI_CTXKV)
           for (int c = n0; c < t_end; c += 128)
-            rope_kv_stage(p, r, seg, row0, c, min(128, t_end - c), p.epi == EPI_CTXKV, tpos + (c - n0), tdst + (c - n0));
-        if (p.epi == EPI_ARGMAX) argmax_stage(p, r, n0, t_end - n0, tpos);   // draft index per token
-        if (p.epi == EPI_QKV || p.epi == EPI_CTXKV || p.epi == EPI_SILU || p.epi == EPI_ARGMAX)
+            rope_kv_stage(p, r, seg, row0, c, min(128, t_end - c), epi == EPI_CTXKV, tpos + (c - n0), tdst + (c - n0));
+        if (epi == EPI_ARGMAX) argmax_stage(p, r, n0, t_end - n0, tpos);   // draft index per token
+        if (epi == EPI_QKV || epi == EPI_CTXKV || epi == EPI_SILU || epi == EPI_ARGMAX)
           row_scales(p, r, n0, t_end - n0, row_sc);
         epi_bar();
       }
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
       const int bar = 1 + half;
       const int off = lo - n0;
       if (lo < hi) {
-        switch (p.epi) {
+        switch (epi) {
           case EPI_QKV:
             epi_rope_kv(p, red, r, seg, row0, lo, hi, sm, row_sc + off, false, tpos + off, tdst + off, 2, bar);
             break;
@@ -254,7 +258,7 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
         }
       }
     }
-    if (p.epi == EPI_ARGMAX) {
+    if (epi == EPI_ARGMAX) {
       // every key of the CTA is in its slots: the last CTA to finish turns the
       // slots into draft ids (half 0)
       epi_pair_bar();
@@ -291,18 +295,18 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
     // on this tile's sums -- the folded-norm row scales and the RoPE positions
     // and KV destinations of the tokens this CTA finishes -- so that only the
     // split-K reduction itself is left after the last CTA of the tile arrives.
-    if (p.epi == EPI_ARGMAX) {
+    if (epi == EPI_ARGMAX) {
       row_scales(p, tid, n0, NT, row_sc);
-    } else if (p.epi != EPI_PARTIAL) {
-      const int members = (p.epi == EPI_SILU ? 2 : 1) * p.splits;
-      const int member = (p.epi == EPI_SILU ? (tile & 1) * p.splits : 0) + split;
+    } else if (epi != EPI_PARTIAL) {
+      const int members = (epi == EPI_SILU ? 2 : 1) * p.splits;
+      const int member = (epi == EPI_SILU ? (tile & 1) * p.splits : 0) + split;
       const int t_end = min(n0 + NT, p.M);
       const int per = (t_end - n0 + members - 1) / members;
       const int lo = min(t_end, n0 + member * per), hi = min(t_end, lo + per);
       if (lo < hi) {
-        if (p.epi == EPI_QKV || p.epi == EPI_CTXKV)
-          rope_kv_stage(p, tid, seg, row0, lo, min(kEpiChunk, hi - lo), p.epi == EPI_CTXKV, tpos, tdst);
-        if (p.epi == EPI_QKV || p.epi == EPI_CTXKV || p.epi == EPI_SILU) row_scales(p, tid, lo, hi - lo, row_sc);
+        if (epi == EPI_QKV || epi == EPI_CTXKV)
+          rope_kv_stage(p, tid, seg, row0, lo, min(kEpiChunk, hi - lo), epi == EPI_CTXKV, tpos, tdst);
+        if (epi == EPI_QKV || epi == EPI_CTXKV || epi == EPI_SILU) row_scales(p, tid, lo, hi - lo, row_sc);
         epi_bar();
       }
     }
@@ -313,7 +317,7 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
       const int grow = row0 + warp * 32 + lane;
       const bool rvalid = grow < p.seg_rows[seg];
       const int gcol = p.seg_col0[seg] + grow;
-      const bool argmax = p.epi == EPI_ARGMAX;
+      const bool argmax = epi == EPI_ARGMAX;
       float* out = p.ws + (size_t)split * p.M * p.N;
       unsigned long long* wkeys = reinterpret_cast<unsigned long long*>(sA);   // [4][NT], ring idle now
       for (int i = 0; i < TT; ++i) {      // token tile i: columns i * XP * BN .., tokens n0 + i * BN ..
@@ -336,25 +340,25 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
                 if (c + j < BN && t < p.M) out[(size_t)t * p.N + gcol] = v[j];
               }
             }
-            continue;
-          }
-          // greedy argmax over this warp's 32 vocabulary rows: packed (logit, lowest id) keys;
-          // token t = b*R + j, anchor rows (j = 0) carry no draft
+          } else {
+            // greedy argmax over this warp's 32 vocabulary rows: packed (logit, lowest id) keys;
+            // token t = b*R + j, anchor rows (j = 0) carry no draft
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (c + j >= BN) break;
-            const int t = n0 + tc + j;
-            const float z = v[j] * row_sc[tc + j];
-            const int jb = p.R > 0 ? t % p.R : 1;
-            const int kidx = p.R > 0 ? (t / p.R) * (p.R - 1) + jb - 1 : t;
-            if (rvalid && p.logits != nullptr && t < p.M && jb != 0) p.logits[(size_t)kidx * p.N + gcol] = z;
-            unsigned long long key = rvalid ? argmax_key(z, (uint32_t)gcol) : 0ull;
+            for (int j = 0; j < 16; ++j) {
+              if (c + j >= BN) break;
+              const int t = n0 + tc + j;
+              const float z = v[j] * row_sc[tc + j];
+              const int jb = p.R > 0 ? t % p.R : 1;
+              const int kidx = p.R > 0 ? (t / p.R) * (p.R - 1) + jb - 1 : t;
+              if (rvalid && p.logits != nullptr && t < p.M && jb != 0) p.logits[(size_t)kidx * p.N + gcol] = z;
+              unsigned long long key = rvalid ? argmax_key(z, (uint32_t)gcol) : 0ull;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
-              key = other > key ? other : key;
+              for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+                key = other > key ? other : key;
+              }
+              if (lane == 0) wkeys[warp * NT + tc + j] = key;
             }
-            if (lane == 0) wkeys[warp * NT + tc + j] = key;
           }
         }
       }
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
           atomicMax(p.argmax_keys + ((size_t)kidx * kKeySlots + (tile % kKeySlots)) * kKeyStride, key);
         }
       }
-      if (p.epi != EPI_PARTIAL) {
+      if (epi != EPI_PARTIAL) {
         epi_bar();   // every epilogue thread's partial sums (or keys) are written
         float* sm = reinterpret_cast<float*>(sA);   // the stage ring is idle now
         if (argmax) {
@@ -399,7 +403,7 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
           }
         } else {
           // all CTAs of the tile (or gate/up pair) meet, then each finishes a slice of tokens
-          const bool pair = p.epi == EPI_SILU;
+          const bool pair = epi == EPI_SILU;
           const int unit = pair ? tile >> 1 : tile;
           const unsigned int idx = (unsigned)(unit * gridDim.x + blockIdx.x);
           const int expected = (pair ? 2 : 1) * p.splits;
@@ -418,7 +422,7 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
             if (lo < hi) {   // row scales and the first chunk's RoPE table were staged above
               const int gcol = p.seg_col0[seg] + row0 + tid;
               const GlobalRed red{&p, {pair ? unit * kTileRows + tid : gcol, pair ? p.seg_rows[0] + unit * kTileRows + tid : gcol}};
-              switch (p.epi) {
+              switch (epi) {
                 case EPI_QKV: epi_rope_kv(p, red, tid, seg, row0, lo, hi, sm, row_sc, false, tpos, tdst, 1); break;
                 case EPI_CTXKV: epi_rope_kv(p, red, tid, seg, row0, lo, hi, sm, row_sc, true, tpos, tdst, 1); break;
                 case EPI_RESID: epi_resid(p, red, tid, tile, seg, row0, lo, hi, sm, true); break;
@@ -706,16 +710,36 @@ size_t gemm_tc_smem_bytes(int BN, int stages, int x_planes, int tt, int w_boxes)
 // CTAs of gemm_tc_kernel resident per SM with `smem` bytes of dynamic shared
 // memory (raises the kernel's shared-memory limit first); 0 on error.
 using GemmKernelFn = void (*)(TcGemmParams);
-static GemmKernelFn gemm_tc_instance(int tt, bool direct) {
-  return tt == 2 ? (direct ? gemm_tc_kernel<2, true> : gemm_tc_kernel<2, false>)
-                 : (direct ? gemm_tc_kernel<1, true> : gemm_tc_kernel<1, false>);
+constexpr int kEpiKinds = 7;   // GemmEpi values
+// instance index: 0 tt 1 split-K with its epilogue compiled in (epi 0..6),
+// 7 tt 1 split-K any epilogue, 8 tt 2 split-K, 9 tt 1 direct, 10 tt 2 direct
+constexpr int kGemmInstances = kEpiKinds + 4;
+static int gemm_tc_index(int tt, bool direct, int epi) {
+  if (direct) return tt == 2 ? kEpiKinds + 3 : kEpiKinds + 2;
+  if (tt == 2) return kEpiKinds + 1;
+  return epi >= 0 && epi < kEpiKinds ? epi : kEpiKinds;
 }
-static cudaError_t gemm_tc_allow_smem(int tt, bool direct, size_t smem) {
-  static size_t allowed[2][3] = {{0, 0, 0}, {0, 0, 0}};
-  if (smem <= allowed[direct][tt]) return cudaSuccess;
+static GemmKernelFn gemm_tc_instance(int idx) {
+  switch (idx) {
+    case EPI_PARTIAL: return gemm_tc_kernel<1, false, EPI_PARTIAL>;
+    case EPI_ARGMAX: return gemm_tc_kernel<1, false, EPI_ARGMAX>;
+    case EPI_QKV: return gemm_tc_kernel<1, false, EPI_QKV>;
+    case EPI_RESID: return gemm_tc_kernel<1, false, EPI_RESID>;
+    case EPI_SILU: return gemm_tc_kernel<1, false, EPI_SILU>;
+    case EPI_Y_SS: return gemm_tc_kernel<1, false, EPI_Y_SS>;
+    case EPI_CTXKV: return gemm_tc_kernel<1, false, EPI_CTXKV>;
+    case kEpiKinds: return gemm_tc_kernel<1, false, -1>;
+    case kEpiKinds + 1: return gemm_tc_kernel<2, false, -1>;
+    case kEpiKinds + 2: return gemm_tc_kernel<1, true, -1>;
+    default: return gemm_tc_kernel<2, true, -1>;
+  }
+}
+static cudaError_t gemm_tc_allow_smem(int idx, size_t smem) {
+  static size_t allowed[kGemmInstances] = {};
+  if (smem <= allowed[idx]) return cudaSuccess;
   const cudaError_t e =
-      cudaFuncSetAttribute(gemm_tc_instance(tt, direct), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess) allowed[direct][tt] = smem;
+      cudaFuncSetAttribute(gemm_tc_instance(idx), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess) allowed[idx] = smem;
   return e;
 }
 
@@ -726,21 +750,22 @@ static cudaError_t gemm_tc_allow_smem(int tt, bool direct, size_t smem) {
 // holds tmem_cols_for(n_cols) of the SM's 512 columns for its whole life, and
 // one that cannot allocate them waits for another to exit, which a split-K
 // partner never does before it; 0 when one CTA does not fit.
-int gemm_tc_resident_ctas(int tt, bool direct, size_t smem, int n_cols) {
-  static cudaFuncAttributes fa_all[2][3];
+int gemm_tc_resident_ctas(int tt, bool direct, size_t smem, int n_cols, int epi) {
+  static cudaFuncAttributes fa_all[kGemmInstances];
   static cudaDeviceProp prop;
-  static bool have[2][3] = {{false, false, false}, {false, false, false}}, have_prop = false;
-  if (gemm_tc_allow_smem(tt, direct, smem) != cudaSuccess) {
+  static bool have[kGemmInstances] = {}, have_prop = false;
+  const int idx = gemm_tc_index(tt, direct, epi);
+  if (gemm_tc_allow_smem(idx, smem) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
-  cudaFuncAttributes* fa = fa_all[direct];
-  if (!have[direct][tt]) {
-    if (cudaFuncGetAttributes(&fa[tt], gemm_tc_instance(tt, direct)) != cudaSuccess) {
+  const cudaFuncAttributes* fa = &fa_all[idx];
+  if (!have[idx]) {
+    if (cudaFuncGetAttributes(&fa_all[idx], gemm_tc_instance(idx)) != cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
-    have[direct][tt] = true;
+    have[idx] = true;
   }
   if (!have_prop) {
     int dev = 0;
@@ -752,9 +777,9 @@ int gemm_tc_resident_ctas(int tt, bool direct, size_t smem, int n_cols) {
   }
   const int threads = direct ? 320 : 192;
   const int warps = threads / 32;
-  const int regs_warp = (fa[tt].numRegs * 32 + 255) / 256 * 256;   // allocated per warp in units of 256
+  const int regs_warp = (fa->numRegs * 32 + 255) / 256 * 256;   // allocated per warp in units of 256
   const int by_regs = prop.regsPerMultiprocessor / (regs_warp * warps);
-  const size_t per_cta = smem + fa[tt].sharedSizeBytes + prop.reservedSharedMemPerBlock;
+  const size_t per_cta = smem + fa->sharedSizeBytes + prop.reservedSharedMemPerBlock;
   const int by_smem = (int)(prop.sharedMemPerMultiprocessor / per_cta);
   const int by_threads = prop.maxThreadsPerMultiProcessor / threads;
   const int by_tmem = 512 / (int)tmem_cols_for(n_cols);
@@ -781,13 +806,14 @@ cudaError_t launch_gemm_tc_persist(const TcGemmParams& p, int grid, cudaStream_t
 }
 
 cudaError_t launch_gemm_tc(const TcGemmParams& p, int n_tiles, int splits, int t_tiles, int stages,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool by_epi) {
   const size_t smem = gemm_tc_smem_bytes(p.BN, stages, p.x_planes, p.tt, p.wpair ? 2 : 1);
   const int tt = p.tt == 2 ? 2 : 1;
   const bool direct = p.direct != 0;
-  cudaError_t e = gemm_tc_allow_smem(tt, direct, smem);
+  const int idx = gemm_tc_index(tt, direct, by_epi ? p.epi : -1);
+  cudaError_t e = gemm_tc_allow_smem(idx, smem);
   if (e != cudaSuccess) return e;
-  e = launch_k(gemm_tc_instance(tt, direct), dim3(t_tiles, n_tiles, splits), dim3(direct ? 320 : 192), smem, s, p);
+  e = launch_k(gemm_tc_instance(idx), dim3(t_tiles, n_tiles, splits), dim3(direct ? 320 : 192), smem, s, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -234,9 +234,11 @@ void launch_argmax_finalize(unsigned long long* keys, int rows, int32_t* ids, cu
 size_t gemm_tc_smem_bytes(int BN, int stages, int x_planes, int tt, int w_boxes = 1);
 size_t gemm_tc_persist_smem_bytes(int BN, int stages, int w_boxes);
 cudaError_t launch_gemm_tc_persist(const TcGemmParams& p, int grid, cudaStream_t s);
-int gemm_tc_resident_ctas(int tt, bool direct, size_t smem, int n_cols);
+// epi / by_epi: the split-K one-tile GEMM has one instance per epilogue (the
+// one in p.epi); -1 / false take the instance that reads it from the parameters
+int gemm_tc_resident_ctas(int tt, bool direct, size_t smem, int n_cols, int epi = -1);
 cudaError_t launch_gemm_tc(const TcGemmParams& p, int n_tiles, int splits, int t_tiles, int stages,
-                           cudaStream_t s);
+                           cudaStream_t s, bool by_epi = true);
 
 template <typename T>
 cudaError_t launch_gemm_simt(const T* x, int ldx, int M, int K, const GemmSegs& segs, int N, float* ws,
