@@ -177,6 +177,7 @@ constexpr int kUItem = 10;       // ints per published item
 // rowK / rowV: the arena rows of the head's K and V at position 0.
 struct UItem {
   int b, split, hk, qt, p_begin, p_end, S, pg, rowK, rowV;
+  int base;   // first block row (every position below it holds context K/V written before this draft)
 };
 
 // Item w of the launch: from the grid (one item per CTA), or the w-th of the
@@ -187,8 +188,11 @@ __device__ __forceinline__ UItem decode_item(const AttnUParams& p, int w) {
   UItem x;
   const int n_hq = p.n_kv * p.n_qtiles;
   int hq;
+  // (the sequence state through L2 only: grid mode may read it before the
+  // dependency wait, when only its release, not a cache flush, orders it
+  // after the kernels that wrote it)
   if constexpr (grid_mode) {
-    x.b = p.seq_order != nullptr ? p.seq_order[blockIdx.z] : blockIdx.z;
+    x.b = p.seq_order != nullptr ? __ldcg(p.seq_order + blockIdx.z) : blockIdx.z;
     x.split = blockIdx.x;
     hq = blockIdx.y;
     x.S = p.n_splits;
@@ -204,9 +208,10 @@ __device__ __forceinline__ UItem decode_item(const AttnUParams& p, int w) {
   x.hk = hq % p.n_kv;
   x.qt = hq / p.n_kv;
   // every load of the sequence's state at once (one round trip)
-  const int cap = p.st.cap[x.b];
-  const int64_t kv_base = p.st.kv_base[x.b];
-  int L = block_base(p.st, x.b) + p.st.rblk[x.b];   // context + this sequence's K_b + 1 block rows
+  const int cap = __ldcg(p.st.cap + x.b);
+  const long long kv_base = __ldcg(reinterpret_cast<const long long*>(p.st.kv_base) + x.b);
+  x.base = p.st.ctx_kv ? __ldcg(p.st.kv_len + x.b) : 0;   // block_base
+  int L = x.base + __ldcg(p.st.rblk + x.b);   // context + this sequence's K_b + 1 block rows
   x.rowK = (int)kv_row(p.kv, kv_base, cap, p.layer, 0, x.hk, 0);
   x.rowV = (int)kv_row(p.kv, kv_base, cap, p.layer, 1, x.hk, 0);
   if (L > cap) {
@@ -221,6 +226,12 @@ __device__ __forceinline__ UItem decode_item(const AttnUParams& p, int w) {
 }
 __device__ __forceinline__ int item_tiles(const UItem& x) {
   return x.p_end > x.p_begin ? (x.p_end - x.p_begin + kUTile - 1) / kUTile : 0;
+}
+// Leading K/V tiles of an item whose whole box lies below the block rows (at
+// most one ring's worth): nothing the predecessor writes is in them.
+__device__ __forceinline__ int early_tiles(const UItem& x) {
+  const int below = (x.base - x.p_begin) / kUTile;
+  return max(0, min(min(below, item_tiles(x)), kUStages));
 }
 
 // Persistent (p.work set): one CTA per SM takes items from the launch's
@@ -307,13 +318,38 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
   // successor CTA that took this SM's columns first would wait for this grid
   // while this CTA waited in its allocation
   pdl_trigger();
-  pdl_wait();   // the queries, the KV arena and the schedule come from the predecessors
-
-  // grid mode: the CTA's one item, decoded by every thread at once
+  // grid mode: the CTA's one item, decoded by every thread at once.  With
+  // early_kv the predecessor released this launch only after its own wait, so
+  // every kernel before it is complete: the item and its leading K/V tiles
+  // below the block rows are read before the wait (the queries and the block
+  // rows' K/V, which the predecessor writes, only after it).
   UItem gx;
-  if constexpr (grid_mode) gx = decode_item<true>(p, 0);
-  bool ok = true;
   int issued = 0, q_loads = 0;   // producers: K (or V) tiles and query tiles whose loads were issued
+  int n_early = 0;
+  if constexpr (grid_mode) {
+    if (p.early_kv) {
+      gx = decode_item<true>(p, 0);
+      n_early = early_tiles(gx);
+      if (lane == 0 && (warp == kWarpQK || warp == kWarpV)) {
+        const bool is_k = warp == kWarpQK;
+        uint64_t* full = is_k ? k_full : v_full;
+        const int row0 = is_k ? gx.rowK : gx.rowV;
+        for (int t = 0; t < n_early; ++t) {   // stage t's first use: no wait for a free slot
+          mbar_arrive_expect_tx(&full[t], 2 * kUBox);
+          uint8_t* dst = ring + (size_t)t * kUStage + (is_k ? 0 : 2 * kUBox);
+          const int pos = gx.p_begin + t * kUTile;
+          tma_load_2d(dst, &p.tm_kv, 0, row0 + pos, &full[t]);
+          tma_load_2d(dst + kUBox, &p.tm_kv, 64, row0 + pos, &full[t]);
+        }
+        issued = n_early;
+      }
+    }
+  }
+  pdl_wait();   // the queries, the KV arena and the schedule come from the predecessors
+  if constexpr (grid_mode) {
+    if (!p.early_kv) gx = decode_item<true>(p, 0);
+  }
+  bool ok = true;
   if (warp == kWarpQK) {
     // ------------------------------------------------ queries and K
     if (lane == 0) {
@@ -335,7 +371,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
             x = decode_item<false>(p, w);
           } else {
             x.b = -1;
-            x.split = x.hk = x.qt = x.p_begin = x.p_end = x.S = x.pg = x.rowK = x.rowV = 0;
+            x.split = x.hk = x.qt = x.p_begin = x.p_end = x.S = x.pg = x.rowK = x.rowV = x.base = 0;
           }
           int* it = items + slot * kUItem;
           it[0] = x.b;
@@ -368,7 +404,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
         tma_load_3d(sQ, &p.tm_q, 0, x.hk * p.G, tok, q_full);
         tma_load_3d(sQ + kUQHalf, &p.tm_q, 64, x.hk * p.G, tok, q_full);
         ++q_loads;
-        for (int t = 0; t < nt; ++t) {
+        for (int t = grid_mode ? n_early : 0; t < nt; ++t) {
           const int g = issued, st = g % kUStages;
           if (!mbar_wait(&k_empty[st], (uint32_t)((g / kUStages) & 1) ^ 1u, abort_flag, p.flags)) {
             ok = false;
@@ -405,7 +441,7 @@ __global__ void __launch_bounds__(kUThreads, 1) attn_umma_kernel(const __grid_co
         }
         const int nt = p_end > p_begin ? (p_end - p_begin + kUTile - 1) / kUTile : 0;
         if (nt == 0) continue;
-        for (int t = 0; t < nt; ++t) {
+        for (int t = grid_mode ? n_early : 0; t < nt; ++t) {
           const int g = issued, st = g % kUStages;
           if (!mbar_wait(&v_empty[st], (uint32_t)((g / kUStages) & 1) ^ 1u, abort_flag, p.flags)) {
             ok = false;

@@ -210,6 +210,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // on neither (weight prefetch, barrier set-up) goes before the wait.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// The dependency wait of a kernel that releases its dependents either at its
+// start (late == 0: the caller triggered already) or only here, after the wait
+// (late != 0).  Released late, a dependent launches only once this kernel's
+// predecessor has completed, and with it (each kernel completes only after its
+// own wait) every kernel before: it may then read, before its own wait,
+// anything those kernels wrote.
+__device__ __forceinline__ void pdl_wait_release(int late) {
+  pdl_wait();
+  if (late) pdl_trigger();
+}
 
 // ---------------------------------------------------------------- TMA
 

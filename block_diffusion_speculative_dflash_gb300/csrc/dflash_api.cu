@@ -350,6 +350,8 @@ struct dflash_ctx {
   int gemm_bn_max = 192;                 // widest plain-operand token tile (MMA N)
   bool gemm_persist = true;              // multi-wave one-split GEMMs on the persistent instance
   bool gemm_by_epi = true;               // split-K one-tile GEMMs on their epilogue's own instance
+  bool attn_early = true;                // grid-mode attention loads its first context K/V before its wait
+  bool attn_early_now = false;           // (set around one layer's attention launch)
   bool lm_fused = false;                 // LM head as one GEMM with the argmax in its epilogue (every M)
   // With fuse_append, an append of <= 128 rows leaves its per-layer K/V
   // projection pending: the next draft's QKV GEMMs take the rows u along (each
@@ -483,6 +485,7 @@ struct GemmOp {
   int rows_max = 0, t0 = 0;
   int* splits_out = nullptr;      // EPI_PARTIAL: receives the number of K splits in ws
   bool trace = true;              // false: the caller traces this launch with what follows it
+  bool late_trigger = false;      // release the dependent launch only after the dependency wait
   // EPI_QKV: the pending context rows u of an append ride along as token tile 1
   // (split bf16 [2][ctx_m][K], folded-norm sums ctx_ss [n_ss][ctx_m]; rows /
   // rows_max as for EPI_CTXKV): their K/V are written with the block's
@@ -658,6 +661,7 @@ int run_gemm_tc(dflash_ctx* c, const void* x, int M, int K, const SegRef* segs, 
   p.xn_gain = reinterpret_cast<const __nv_bfloat16*>(op.xn_gain);
   p.eps = c->cfg.rms_eps;
   p.epi = op.epi;
+  p.late_trigger = op.late_trigger ? 1 : 0;
   p.counters = c->d_counters;
   p.argmax_keys = c->d_keys;
   p.logits = op.logits;
@@ -949,6 +953,7 @@ int run_attention_umma(dflash_ctx* c, const void* qb, void* ob, int l, int R, cu
   p.n_splits = (int)std::max<int64_t>(1, std::min<int64_t>(64, (max_tiles + per_cta - 1) / per_cta));
   p.n_splits = clamp_splits_to_scratch(c, p.n_splits, (size_t)c->B * p.n_kv * p.rows_pad);
   if (c->plan_mode == 1) p.seq_order = c->d_seq_order;   // longest contexts first
+  p.early_kv = c->attn_early_now ? 1 : 0;
   if (p.n_splits > 1)
     RET(attn_workspace(c, (size_t)c->B * p.n_kv * p.n_splits * p.rows_pad, &p.part_o, &p.part_lse, s));
   CK(launch_attention_umma(p, c->B, 0, s));
@@ -1247,14 +1252,23 @@ int draft_bf16(dflash_ctx* c, const int32_t* anchor_dev, int K, float* logits_de
     L.od = L.oo;
     L.od.xn_gain = l + 1 < c->nl ? c->w.layers[l + 1].attn_norm : c->w.final_norm;
   };
+  // A grid-mode tcgen05 attention loads its first context K/V tiles before its
+  // dependency wait: its QKV GEMM then releases it only after its own wait (so
+  // every kernel before the GEMM is complete) and must write no K/V below the
+  // block rows (no pending append rides along).
+  const bool early_kv = c->attn_early && !fuse_ctx && c->plan_mode != 2 && attention_on_umma(c);
   LayerOps L[2];
   build(0, L[0]);
   for (int l = 0; l < c->nl; ++l) {
     LayerOps& cur = L[l & 1];
     LayerOps& nxt = L[(l + 1) & 1];
     if (l + 1 < c->nl) build(l + 1, nxt);
+    cur.oq.late_trigger = early_kv;
     RET(run_gemm_tc(c, xn, M, H, cur.qkv, 3, cur.oq, s));
-    RET(run_attention<bf>(c, reinterpret_cast<const bf*>(c->qb), reinterpret_cast<bf*>(c->ob), l, R, s));
+    c->attn_early_now = early_kv;
+    const int ra = run_attention<bf>(c, reinterpret_cast<const bf*>(c->qb), reinterpret_cast<bf*>(c->ob), l, R, s);
+    c->attn_early_now = false;
+    RET(ra);
     RET(run_gemm_tc(c, c->ob, M, c->q_dim, cur.wo, 1, cur.oo, s));
     RET(run_gemm_tc(c, xn, M, H, cur.gu, 2, cur.og, s));
     RET(run_gemm_tc(c, c->ab, M, c->I, cur.wd, 1, cur.od, s));
@@ -1719,6 +1733,8 @@ static int create_impl(const dflash_config* cfg, const dflash_weights* w, int32_
     if (gpe && gpe[0] == '0') c->gemm_persist = false;
     const char* gei = getenv("DFLASH_GEMM_BY_EPI");   // 0: one split-K instance reads the epilogue at run time
     if (gei && gei[0] == '0') c->gemm_by_epi = false;
+    const char* ae = getenv("DFLASH_ATTN_EARLY");   // 0: every attention load after the dependency wait
+    if (ae && ae[0] == '0') c->attn_early = false;
     const char* gb = getenv("DFLASH_GEMM_BN_MAX");   // widest plain token tile, 64..256 in steps of 16
     if (gb) c->gemm_bn_max = std::max(64, std::min(256, atoi(gb) / 16 * 16));
     const char* gc = getenv("DFLASH_GEMM_CTAS");

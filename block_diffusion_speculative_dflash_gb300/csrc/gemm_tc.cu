@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
   int* tpos = reinterpret_cast<int*>(tdst + kStageTok);            // [kStageTok] RoPE positions
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_trigger();
+  if (!p.late_trigger) pdl_trigger();   // (else after the dependency wait)
 
   // weight tile -> segment
   // grid (token tiles, weight tiles, splits): the token tiles of one weight tile
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
                            &full[kb], pol);
       }
       issued = pre;
-      pdl_wait();
+      pdl_wait_release(p.late_trigger);
       tma_prefetch_desc(&p.tm_x);
       if (TT == 2 && p.fuse_ctx) tma_prefetch_desc(&p.tm_x2);
       for (int kb = 0; kb < nkb; ++kb) {
@@ -171,10 +171,10 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
         }
       }
     } else {
-      pdl_wait();
+      pdl_wait_release(p.late_trigger);
     }
   } else if (warp == EW + 1) {
-    pdl_wait();
+    pdl_wait_release(p.late_trigger);
     if (lane == 0) {
       // fp16 token operands go with the fp16 weight copies (A and B of one type)
       const uint32_t idesc = p.op16 ? umma_idesc_f16(kTileRows, XP * BN) : umma_idesc_bf16(kTileRows, XP * BN);
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
     // epilogue warps, two per tensor-memory lane quadrant (warp w reads lanes
     // 32 (w % 4) ..): half h = w / 4 finishes its own contiguous run of whole
     // token chunks, on its own named barrier and scratch.
-    pdl_wait();
+    pdl_wait_release(p.late_trigger);
     const int half = warp >> 2;
     const int r = threadIdx.x & 127;   // tile row = tensor-memory lane
     const int t_end = min(n0 + NT, p.M);
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(DIRECT ? 320 : 192, TT == 1 && !DIRECT ? 2 : 1
       }
     }
   } else {
-    pdl_wait();
+    pdl_wait_release(p.late_trigger);
     const int tid = threadIdx.x;   // 0..127
     // While the weights stream: everything of the epilogue that does not depend
     // on this tile's sums -- the folded-norm row scales and the RoPE positions
@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(320, 1) gemm_tc_persist_kernel(const __grid_co
   int* tpos = reinterpret_cast<int*>(tdst + kStageTok);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_trigger();
+  if (!p.late_trigger) pdl_trigger();   // (else after the dependency wait)
   const int T = p.p_tiles, TX = p.p_ttiles;   // tiles, token tiles per weight tile
   const uint32_t ncols = tmem_cols_for(BN * W);   // one accumulator
   auto decode = [&](int tau, int& tile, int& seg, int& row0, int& n0) {
@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(320, 1) gemm_tc_persist_kernel(const __grid_co
                              pol);
         }
       }
-      pdl_wait();
+      pdl_wait_release(p.late_trigger);
       tma_prefetch_desc(&p.tm_x);
       int g = 0;
       for (int tau = blockIdx.x; tau < T && ok; tau += gridDim.x) {
@@ -583,10 +583,10 @@ __global__ void __launch_bounds__(320, 1) gemm_tc_persist_kernel(const __grid_co
         }
       }
     } else {
-      pdl_wait();
+      pdl_wait_release(p.late_trigger);
     }
   } else if (warp == EW + 1) {
-    pdl_wait();
+    pdl_wait_release(p.late_trigger);
     if (lane == 0) {
       const uint32_t idesc = p.op16 ? umma_idesc_f16(kTileRows, BN) : umma_idesc_bf16(kTileRows, BN);
       int g = 0, j = 0;
@@ -624,7 +624,7 @@ __global__ void __launch_bounds__(320, 1) gemm_tc_persist_kernel(const __grid_co
     // eight epilogue warps, two per tensor-memory lane quadrant, as in the
     // one-tile direct instance; between tiles both halves meet, then the
     // accumulator is handed back to the MMA issuer
-    pdl_wait();
+    pdl_wait_release(p.late_trigger);
     const int half = warp >> 2;
     const int r = threadIdx.x & 127;
     int j = 0;

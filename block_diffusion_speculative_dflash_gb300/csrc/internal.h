@@ -164,6 +164,8 @@ struct TcGemmParams : EpiArgs {
   int wpair;                    // 1 (EPI_SILU, direct, tt = 1): CTA y computes gate tile y and up
                                 //    tile y (two weight boxes per stage, two accumulators)
   int p_tiles, p_ttiles;        // persistent instance: tiles, token tiles per weight tile
+  int late_trigger;             // 1: the dependent launch is released after the dependency wait
+                                //    (its pre-wait reads may then see every earlier kernel's writes)
 };
 
 
@@ -209,6 +211,10 @@ struct AttnUParams {
   float scale_log2;
   uint32_t* flags;
   size_t o_plane;
+  // grid mode: the predecessor (the layer's QKV GEMM) released this launch
+  // after its own dependency wait and writes no K/V below block_base, so the
+  // first K/V tiles below it may be loaded before this kernel's wait
+  int early_kv;
 };
 size_t attn_umma_smem_bytes();
 cudaError_t launch_attention_umma(const AttnUParams& p, int B, int grid, cudaStream_t s);
