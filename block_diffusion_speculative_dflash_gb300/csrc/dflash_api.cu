@@ -537,13 +537,20 @@ GemmPlan plan_gemm(const dflash_ctx* c, int M, int K, const SegRef* segs, int ns
   // stages of narrow token tiles in 100 KB each, or 3 stages of tiles up to 160
   // columns in 110 KB each (measured faster than one CTA with 6 stages); one
   // CTA with a deep ring otherwise
+  // The LM head's narrow partial-store tiles (1187 weight tiles at the
+  // Qwen3-4B shape) stream best four CTAs to an SM with two stages each: a
+  // CTA's turnover then stalls a quarter of the SM's loads in flight instead
+  // of half (17 rows: 125.2 -> 121.1 us; the projections measured slower so).
   const int n_cols = g.tt * g.XP * g.BN;
-  int ctas_per_sm = c->gemm_ctas > 0                        ? c->gemm_ctas
-                    : n_cols <= 64                           ? 2
-                    : (op.ctx_x != nullptr && 4 * g.BN <= 128) ? 2
-                    : 3 * stage_bytes <= (110 << 10) - 4096  ? 2
-                                                             : 1;
-  const int budget_kb = ctas_per_sm == 2 ? (n_cols <= 64 || op.ctx_x != nullptr ? 100 : 110) : 212;
+  int ctas_per_sm = c->gemm_ctas > 0                             ? c->gemm_ctas
+                    : op.epi == EPI_PARTIAL && n_cols <= 64       ? 4
+                    : n_cols <= 64                                ? 2
+                    : (op.ctx_x != nullptr && 4 * g.BN <= 128)      ? 2
+                    : 3 * stage_bytes <= (110 << 10) - 4096       ? 2
+                                                                  : 1;
+  const int budget_kb = ctas_per_sm == 4   ? 54
+                        : ctas_per_sm == 2 ? (n_cols <= 64 || op.ctx_x != nullptr ? 100 : 110)
+                                           : 212;
   const int budget = (c->gemm_smem_kb > 0 ? c->gemm_smem_kb : budget_kb) * 1024;
   g.stages = std::max(2, std::min(8, budget / stage_bytes));
   // the split CTAs of a tile wait for each other in the epilogue, so a split
