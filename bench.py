@@ -77,6 +77,44 @@ def lm_traffic(s, K):
         return None
 
 
+def other_config_cmd(name, steps=8, warmup=3):
+    """The bench command of another workload, run in a child process beside the headline
+    (the same script and path, its own CUDA context; no CPU baseline, e2e or K sweep)."""
+    return [sys.executable, os.path.abspath(__file__), "--config", name, "--steps", str(steps),
+            "--warmup", str(warmup), "--no-cpu-baseline", "--no-e2e", "--k-sweep=", "--other-configs="]
+
+
+def other_config_summary(name, rc, stdout, stderr=""):
+    """What the headline line reports of another workload's run: its step time, blocks/s,
+    clocks and workload from the last JSON line the child printed, or why there is none."""
+    line = None
+    for text in reversed((stdout or "").splitlines()):
+        text = text.strip()
+        if text.startswith("{"):
+            try:
+                line = json.loads(text)
+                break
+            except ValueError:
+                continue
+    if rc != 0 or line is None or "ms_per_step" not in line:
+        tail = " | ".join(((stderr or "") + "\n" + (stdout or "")).strip().splitlines()[-3:])
+        return {"error": f"exit {rc}: {tail}"[:300]}
+    return {"us_per_step": line["ms_per_step"] * 1e3, "blocks_per_s": line["value"],
+            "clocks": line.get("clocks"), "workload": line.get("config", {}).get("workload"),
+            "command": " ".join(["python bench.py"] + other_config_cmd(name)[2:])}
+
+
+def run_other_configs(names, timeout=300):
+    out = {}
+    for name in names:
+        try:
+            r = subprocess.run(other_config_cmd(name), capture_output=True, text=True, timeout=timeout, cwd=ROOT)
+            out[name] = other_config_summary(name, r.returncode, r.stdout, r.stderr)
+        except Exception as e:   # (a timeout or a failed start: reported, not fatal to the headline)
+            out[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
+    return out
+
+
 def aggregate_ranks(ms_da, ms_it, B, world, device="cpu"):
     """Whole-job figures over `world` ranks that each ran their own batch of B
     independent sequences: the step time is the slowest rank's (max over ranks),
@@ -385,6 +423,9 @@ def main():
                     help="override the workload's batch (a smaller case, e.g. for a profiler capture)")
     ap.add_argument("--ctx-max", type=int, default=None,
                     help="cap the workload's context lengths (a smaller case, e.g. for a profiler capture)")
+    ap.add_argument("--other-configs", default="llama31_8b,qwen3_4b_serving",
+                    help="workloads also timed, each in a child process, and reported under "
+                         "'other_configs' of the headline line ('' to skip)")
     ap.add_argument("--conditioning", default="kv", choices=["kv", "input", "none"],
                     help="how the target context conditions the draft: K/V injection (the method), "
                          "input fusion or none (the ablation variants)")
@@ -665,6 +706,12 @@ def main():
         torch.cuda.synchronize()
         out["k_sweep"] = k_sweep_bench(Wd, [int(k) for k in args.k_sweep.split(",")], steps=min(args.steps, 10),
                                        warmup=3)
+
+    # ---- the other workloads' steps, each in a child process (rank 0, N=1 only) --------
+    if args.other_configs and args.config == "qwen3_4b" and args.conditioning == "kv" and world == 1:
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        out["other_configs"] = run_other_configs([n for n in args.other_configs.split(",") if n])
 
     # ---- CPU oracle baseline on a bounded sample (rank 0, N=1 only) -----------------
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

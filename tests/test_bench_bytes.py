@@ -56,3 +56,29 @@ def test_lm_traffic_only_for_current_sources(monkeypatch):
     assert bench.lm_traffic(Shape, 16) is None
     monkeypatch.undo()
     assert bench.lm_traffic(Shape, 32) is None   # another workload
+
+
+def test_other_config_summary_reads_the_childs_last_line():
+    import json
+
+    import bench
+    line = {"metric": "m", "value": 8367.5, "ms_per_step": 0.9561, "clocks": {"sm_mhz": 2070.0},
+            "config": {"workload": "llama31_8b: ..."}}
+    out = "warming up\n" + json.dumps({"value": 1.0}) + "\n" + json.dumps(line) + "\n"
+    r = bench.other_config_summary("llama31_8b", 0, out)
+    assert r["us_per_step"] == pytest.approx(956.1) and r["blocks_per_s"] == 8367.5
+    assert r["workload"] == "llama31_8b: ..." and r["clocks"] == {"sm_mhz": 2070.0}
+    assert r["command"].startswith("python bench.py --config llama31_8b ")
+    # a failed child or one without a result line is reported, not raised
+    assert "error" in bench.other_config_summary("x", 1, json.dumps(line), "Traceback\nRuntimeError: boom")
+    assert "boom" in bench.other_config_summary("x", 1, "", "Traceback\nRuntimeError: boom")["error"]
+    assert "error" in bench.other_config_summary("x", 0, "no json here\n{not json")
+
+
+def test_other_config_cmd_runs_no_nested_extras():
+    import bench
+    cmd = bench.other_config_cmd("qwen3_4b_serving")
+    assert cmd[1].endswith("bench.py") and cmd[cmd.index("--config") + 1] == "qwen3_4b_serving"
+    for flag in ("--no-cpu-baseline", "--no-e2e", "--k-sweep=", "--other-configs="):
+        assert flag in cmd
+    assert int(cmd[cmd.index("--warmup") + 1]) >= 3
